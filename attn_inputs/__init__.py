@@ -1,0 +1,129 @@
+"""Seeded synthetic inputs for attention, shared by the CUDA path's tests/bench
+and by the CPU oracle.
+
+This module holds no attention arithmetic: it only draws numbers.  The
+workloads use Q, K, V drawn i.i.d. from N(0, 1) (optionally scaled, e.g. keys
+x3 for the long-context stress case) and rounded to fp16 or bf16.
+
+Generator (counter-based, so any element can be drawn independently and the
+x86 and aarch64 hosts agree):
+
+* splitmix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014): output n of stream ``seed`` is
+  ``mix64(seed + (n + 1) * 0x9E3779B97F4A7C15)`` with the published finaliser
+  ``mix64``.
+* 53-bit uniforms in the open interval (0, 1): ``((x >> 11) + 0.5) * 2**-53``.
+* Box-Muller (Box & Muller, 1958): element pair (2k, 2k+1) takes uniforms
+  u1 = U(2k), u2 = U(2k+1) and gives r*cos(2*pi*u2), r*sin(2*pi*u2) with
+  r = sqrt(-2 ln u1).
+* The float64 normal times ``scale`` is rounded once (round-to-nearest-even)
+  to the storage dtype by torch's CPU conversion.
+
+Seeds follow ``seed = 1000 * config_id + 10 * layer + {0: Q, 1: K, 2: V}``.
+"""
+from __future__ import annotations
+
+import hashlib
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 22  # pairs per chunk (bounds temporaries to ~32 MB each)
+
+GENERATOR_VERSION = "splitmix64-boxmuller-v1"
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
+    """Outputs ``start .. start+count-1`` of the splitmix64 stream ``seed``."""
+    n = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + n * GAMMA)
+
+
+def uniform53(x: np.ndarray) -> np.ndarray:
+    return ((x >> np.uint64(11)).astype(np.float64) + 0.5) * (2.0 ** -53)
+
+
+def normal_f64(seed: int, numel: int) -> np.ndarray:
+    """``numel`` i.i.d. N(0,1) float64 values of stream ``seed``."""
+    out = np.empty(numel, dtype=np.float64)
+    npairs = (numel + 1) // 2
+    for p0 in range(0, npairs, _CHUNK):
+        p1 = min(npairs, p0 + _CHUNK)
+        u = uniform53(splitmix64(seed, 2 * p0, 2 * (p1 - p0)))
+        u1, u2 = u[0::2], u[1::2]
+        r = np.sqrt(-2.0 * np.log(u1))
+        t = (2.0 * math.pi) * u2
+        pair = np.empty(2 * (p1 - p0), dtype=np.float64)
+        pair[0::2] = r * np.cos(t)
+        pair[1::2] = r * np.sin(t)
+        e0, e1 = 2 * p0, min(numel, 2 * p1)
+        out[e0:e1] = pair[: e1 - e0]
+    return out
+
+
+def normal_tensor(seed: int, shape, dtype: str, scale: float = 1.0) -> torch.Tensor:
+    """A CPU tensor of ``shape`` drawn from stream ``seed``, times ``scale``,
+    rounded once to ``dtype`` ("fp16" | "bf16" | "f64")."""
+    numel = int(np.prod(shape)) if len(shape) else 1
+    z = normal_f64(seed, numel)
+    if scale != 1.0:
+        z = z * scale
+    t = torch.from_numpy(z).reshape(tuple(shape))
+    if dtype == "f64":
+        return t
+    return t.to(DTYPES[dtype])
+
+
+def seed_for(config_id: int, layer: int, which: str) -> int:
+    return 1000 * config_id + 10 * layer + {"Q": 0, "K": 1, "V": 2}[which]
+
+
+@dataclass(frozen=True)
+class AttnShape:
+    """One attention call: Q,O (B,Hq,Nq,d); K,V (B,Hkv,Nk,d)."""
+
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str = "fp16"
+    causal: bool = False
+    window: int = 0
+    sm_scale: float | None = None
+    key_scale: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(self.d)
+
+
+def make_qkv(shape: AttnShape, config_id: int = 0, layer: int = 0):
+    """Seeded (Q, K, V) CPU tensors in the storage dtype, contiguous."""
+    q = normal_tensor(seed_for(config_id, layer, "Q"), (shape.B, shape.Hq, shape.Nq, shape.d), shape.dtype)
+    k = normal_tensor(seed_for(config_id, layer, "K"), (shape.B, shape.Hkv, shape.Nk, shape.d), shape.dtype,
+                      scale=shape.key_scale)
+    v = normal_tensor(seed_for(config_id, layer, "V"), (shape.B, shape.Hkv, shape.Nk, shape.d), shape.dtype)
+    return q, k, v
+
+
+def sha256_of(t: torch.Tensor) -> str:
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    return hashlib.sha256(t.numpy().tobytes()).hexdigest()

@@ -1,0 +1,201 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU attention: the correctness oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path and must never be used as a
+ * fallback for it.
+ *
+ * What it computes is the plain definition of scaled dot-product attention,
+ * written out with no tiling, no online softmax and no reordering:
+ *
+ *   "Bloque C -- implementar la referencia" (lab 02 page, lynx-cortex
+ *   phase-27 "Forward de flash attention en Triton"): S = Q K^T * sm_scale,
+ *   masked entries set to -inf, P = softmax(S) row by row, O = P V;
+ *   and the "standard attention" half of the worked example in
+ *   "FlashAttention: Nunca materializar la matriz de atencion" (cruxr.ai,
+ *   "Optimizaciones de Atencion"): the full score row, its maximum, the
+ *   exponentials shifted by that maximum, their sum, the normalised weights
+ *   and the weighted sum of V rows.
+ *
+ * Per query row i of head h in batch b (Q,O: B x Hq x Nq x d; K,V: B x Hkv x
+ * Nk x d; all row-major):
+ *   1. kvh = h / (Hq / Hkv)                       (consecutive GQA grouping)
+ *   2. p   = Nk - Nq + i                           (bottom-right alignment)
+ *   3. key j is live iff (!causal || j <= p) && (window <= 0 || p - j < window)
+ *      (causal keeps j <= i, "position i attends to itself", lab 02 "Errores
+ *       tipicos"; the sliding window keeps the last `window` tokens, motivation
+ *       page "Otras tres variantes de attention")
+ *   4. s_j = sm_scale * sum_k Q[b,h,i,k] K[b,kvh,j,k] for live j, -inf else
+ *   5. M = max_j s_j, w_j = exp(s_j - M), l = sum_j w_j  (batch softmax)
+ *   6. O[b,h,i,:] = sum_j (w_j / l) V[b,kvh,j,:]
+ *   7. LSE[b,h,i] = M + ln(l)   (natural log of the sum of exp of the scaled,
+ *      masked scores; lab 02 kernel skeleton stores m + log(l))
+ * A row with no live key has no defined softmax; the oracle returns NaN for
+ * its O and -inf for its LSE so that any comparison against it fails.
+ *
+ * Arithmetic is IEEE fp64 with the host libm's exp/log, compiled without
+ * -ffast-math; rows run in parallel with OpenMP, each row sequentially.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ENOMEM -2
+
+static int key_is_live(long p, long j, int causal, int window) {
+  if (causal && j > p) return 0;
+  if (window > 0 && p - j >= window) return 0;
+  return 1;
+}
+
+/* One query row: q (d), Kh/Vh (Nk x d) of its kv head, scratch s (Nk). */
+static void attend_one_row(const double *q, const double *Kh, const double *Vh,
+                           long Nq, long Nk, long d, long i, int causal,
+                           int window, double sm_scale, double *s, double *o,
+                           double *lse) {
+  const long p = Nk - Nq + i;
+  double M = -INFINITY;
+  for (long j = 0; j < Nk; ++j) {
+    if (!key_is_live(p, j, causal, window)) {
+      s[j] = -INFINITY;
+      continue;
+    }
+    const double *k = Kh + j * d;
+    double dot = 0.0;
+    for (long c = 0; c < d; ++c) dot += q[c] * k[c];
+    s[j] = sm_scale * dot;
+    if (s[j] > M) M = s[j];
+  }
+  if (M == -INFINITY) { /* empty live set */
+    for (long c = 0; c < d; ++c) o[c] = NAN;
+    *lse = -INFINITY;
+    return;
+  }
+  double l = 0.0;
+  for (long j = 0; j < Nk; ++j) {
+    const double w = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - M);
+    s[j] = w;
+    l += w;
+  }
+  for (long c = 0; c < d; ++c) o[c] = 0.0;
+  for (long j = 0; j < Nk; ++j) {
+    if (s[j] == 0.0) continue;
+    const double pj = s[j] / l;
+    const double *v = Vh + j * d;
+    for (long c = 0; c < d; ++c) o[c] += pj * v[c];
+  }
+  *lse = M + log(l);
+}
+
+static int check_args(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                      double sm_scale) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0)
+    return ORACLE_EINVAL;
+  if (Hq % Hkv != 0) return ORACLE_EINVAL;
+  if (!(sm_scale > 0.0) || isinf(sm_scale)) return ORACLE_EINVAL;
+  return ORACLE_OK;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Full attention: every (b, h, i).  LSE may be NULL.  nthreads <= 0 uses the
+ * OpenMP default.  Returns 0, or a negative code on bad arguments / no memory. */
+int oracle_attn_fwd(const double *Q, const double *K, const double *V,
+                    double *O, double *LSE, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, int causal, int window, double sm_scale,
+                    int nthreads) {
+  int rc = check_args(B, Hq, Hkv, Nq, Nk, d, sm_scale);
+  if (rc) return rc;
+  if (!Q || !K || !V || !O) return ORACLE_EINVAL;
+  const long rows = (long)B * Hq * Nq;
+  const int g = Hq / Hkv;
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+    if (!s) {
+      failed = 1;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16)
+#endif
+      for (long r = 0; r < rows; ++r) {
+        const long i = r % Nq;
+        const long bh = r / Nq;
+        const long h = bh % Hq;
+        const long b = bh / Hq;
+        const long kvh = h / g;
+        const double *Kh = K + ((b * Hkv + kvh) * (long)Nk) * d;
+        const double *Vh = V + ((b * Hkv + kvh) * (long)Nk) * d;
+        double lse;
+        attend_one_row(Q + r * d, Kh, Vh, Nq, Nk, d, i, causal, window,
+                       sm_scale, s, O + r * d, &lse);
+        if (LSE) LSE[r] = lse;
+      }
+      free(s);
+    }
+  }
+  return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
+/* Selected rows only.  row_ids[n] is the flat index (b*Hq + h)*Nq + i of a
+ * query row; Qrows holds those rows' Q vectors (n x d), in the same order.
+ * O (n x d) and LSE (n) receive the results. */
+int oracle_attn_rows(const double *Qrows, const int64_t *row_ids, long n,
+                     const double *K, const double *V, double *O, double *LSE,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     int window, double sm_scale, int nthreads) {
+  int rc = check_args(B, Hq, Hkv, Nq, Nk, d, sm_scale);
+  if (rc) return rc;
+  if (!Qrows || !row_ids || !K || !V || !O || n < 0) return ORACLE_EINVAL;
+  const long rows = (long)B * Hq * Nq;
+  for (long t = 0; t < n; ++t)
+    if (row_ids[t] < 0 || row_ids[t] >= rows) return ORACLE_EINVAL;
+  const int g = Hq / Hkv;
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+    if (!s) {
+      failed = 1;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+      for (long t = 0; t < n; ++t) {
+        const long r = (long)row_ids[t];
+        const long i = r % Nq;
+        const long bh = r / Nq;
+        const long h = bh % Hq;
+        const long b = bh / Hq;
+        const long kvh = h / g;
+        const double *Kh = K + ((b * Hkv + kvh) * (long)Nk) * d;
+        const double *Vh = V + ((b * Hkv + kvh) * (long)Nk) * d;
+        double lse;
+        attend_one_row(Qrows + t * d, Kh, Vh, Nq, Nk, d, i, causal, window,
+                       sm_scale, s, O + t * d, &lse);
+        if (LSE) LSE[t] = lse;
+      }
+      free(s);
+    }
+  }
+  return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
