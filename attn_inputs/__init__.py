@@ -25,6 +25,8 @@ from __future__ import annotations
 
 import hashlib
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -57,21 +59,33 @@ def uniform53(x: np.ndarray) -> np.ndarray:
     return ((x >> np.uint64(11)).astype(np.float64) + 0.5) * (2.0 ** -53)
 
 
+def _fill_chunk(out: np.ndarray, seed: int, numel: int, p0: int, p1: int) -> None:
+    u = uniform53(splitmix64(seed, 2 * p0, 2 * (p1 - p0)))
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = (2.0 * math.pi) * u2
+    pair = np.empty(2 * (p1 - p0), dtype=np.float64)
+    pair[0::2] = r * np.cos(t)
+    pair[1::2] = r * np.sin(t)
+    e0, e1 = 2 * p0, min(numel, 2 * p1)
+    out[e0:e1] = pair[: e1 - e0]
+
+
 def normal_f64(seed: int, numel: int) -> np.ndarray:
-    """``numel`` i.i.d. N(0,1) float64 values of stream ``seed``."""
+    """``numel`` i.i.d. N(0,1) float64 values of stream ``seed``.
+
+    Chunks are independent (counter-based), so they are filled by a thread
+    pool; the result does not depend on the number of threads."""
     out = np.empty(numel, dtype=np.float64)
     npairs = (numel + 1) // 2
-    for p0 in range(0, npairs, _CHUNK):
-        p1 = min(npairs, p0 + _CHUNK)
-        u = uniform53(splitmix64(seed, 2 * p0, 2 * (p1 - p0)))
-        u1, u2 = u[0::2], u[1::2]
-        r = np.sqrt(-2.0 * np.log(u1))
-        t = (2.0 * math.pi) * u2
-        pair = np.empty(2 * (p1 - p0), dtype=np.float64)
-        pair[0::2] = r * np.cos(t)
-        pair[1::2] = r * np.sin(t)
-        e0, e1 = 2 * p0, min(numel, 2 * p1)
-        out[e0:e1] = pair[: e1 - e0]
+    starts = list(range(0, npairs, _CHUNK))
+    if len(starts) <= 1:
+        for p0 in starts:
+            _fill_chunk(out, seed, numel, p0, min(npairs, p0 + _CHUNK))
+        return out
+    workers = min(len(starts), os.cpu_count() or 1, 32)
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda p0: _fill_chunk(out, seed, numel, p0, min(npairs, p0 + _CHUNK)), starts))
     return out
 
 
@@ -127,3 +141,35 @@ def sha256_of(t: torch.Tensor) -> str:
     if t.dtype == torch.bfloat16:
         t = t.view(torch.int16)
     return hashlib.sha256(t.numpy().tobytes()).hexdigest()
+
+
+# ---------------------------------------------------------------- workloads
+# The synthetic workloads (shapes, dtypes, masks, seeds).  config_id numbers
+# them in a fixed order and feeds the seed rule above.
+def workload_calls(name: str):
+    """List of ``(AttnShape, config_id, layer)`` for a named workload."""
+    if name == "mha_n64":  # smallest instance: B=1, H=2, N=64, d=64, fp16
+        return [(AttnShape(1, 2, 2, 64, 64, 64, "fp16", c, 0, 0.125), 0, int(c)) for c in (False, True)]
+    if name == "mha_b2h4":  # B=2, H=4, d=64, fp16, N in {256, 1024, 4096} x causal
+        out = []
+        for li, n in enumerate((256, 1024, 4096)):
+            for c in (True, False):
+                out.append((AttnShape(2, 4, 4, n, n, 64, "fp16", c, 0, None), 1, 2 * li + int(c)))
+        return out
+    if name == "gpt_stack":  # 12 layers of B=8, H=12, N=2048, d=64, bf16, causal, scale 1/8
+        return [(AttnShape(8, 12, 12, 2048, 2048, 64, "bf16", True, 0, 0.125), 2, layer) for layer in range(12)]
+    if name == "gqa_mqa":  # B=4, Hq=32, Hkv in {8, 1}, N=8192, d=128, bf16, causal; + window 4096
+        return [(AttnShape(4, 32, 8, 8192, 8192, 128, "bf16", True, 0, None), 3, 0),
+                (AttnShape(4, 32, 1, 8192, 8192, 128, "bf16", True, 0, None), 3, 1),
+                (AttnShape(4, 32, 8, 8192, 8192, 128, "bf16", True, 4096, None), 3, 2)]
+    if name == "long_prefill":  # B=1, Hq=32, Hkv=8, N=32768, d=128, bf16, keys x3, causal
+        return [(AttnShape(1, 32, 8, 32768, 32768, 128, "bf16", True, 0, None, key_scale=3.0), 4, 0)]
+    if name == "mqa_decode":  # one decode step: B=4, Hq=32, Hkv in {1, 8}, Nq=1, Nk=8192, d=128, bf16
+        return [(AttnShape(4, 32, 1, 1, 8192, 128, "bf16", True, 0, None), 5, 0),
+                (AttnShape(4, 32, 8, 1, 8192, 128, "bf16", True, 0, None), 5, 1)]
+    if name == "mha_n64_bw":  # bandwidth-sized sibling of mha_n64: B=512, H=32, N=64, d=64, fp16
+        return [(AttnShape(512, 32, 32, 64, 64, 64, "fp16", c, 0, 0.125), 6, int(c)) for c in (False, True)]
+    raise KeyError(name)
+
+
+WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw"]

@@ -1,0 +1,481 @@
+#!/usr/bin/env python
+"""Benchmark: attention-forward TFLOP/s on one GB300 and the roofline fraction
+of the dominant kernel, next to the fp64 CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass over every call of the workload (default ``mha_b2h4``:
+B=2, H=4, d=64, fp16, N in {256, 1024, 4096} x causal in {true, false}) with
+inputs resident in HBM.  The step is captured once as a CUDA graph and
+replayed; L2 is flushed (a 256 MiB write) between timed steps, outside the
+timed events.  Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import attn_inputs as ai  # noqa: E402
+from tiled_attention_forward_fwd_gb300 import accounting as acc  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_TEXT = {
+    "mha_b2h4": "MHA forward B=2, H=4, d=64, fp16, N in {256,1024,4096} x causal in {true,false}",
+    "mha_n64": "MHA forward B=1, H=2, N=64, d=64, fp16, causal in {false,true}",
+    "gpt_stack": "12 causal layers B=8, H=12, N=2048, d=64, bf16, scale 1/8",
+    "gqa_mqa": "B=4, Hq=32, Hkv in {8,1}, N=8192, d=128, bf16, causal; + window 4096",
+    "long_prefill": "B=1, Hq=32, Hkv=8, N=32768, d=128, bf16, keys x3, causal",
+    "mqa_decode": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16",
+    "mha_n64_bw": "MHA forward B=512, H=32, N=64, d=64, fp16, causal in {false,true}",
+}
+KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "sm103_ptx.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mha_b2h4", choices=ai.WORKLOAD_NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--per-call", action="store_true", help="print per-call timings to stderr")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing (weak scaling, no collective
+# on the data path: every rank runs the same workload on its own GPU)
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def dist_max(ws, x: float, device) -> float:
+    if ws <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks, clocks, profiles
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = []
+        for i, n in enumerate(names):
+            if any(r[5 + i].lower() == "active" for r in self.rows):
+                reasons.append(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tiled_attention_forward_fwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, call_label: str):
+    """DRAM bytes per launch from a committed ncu summary, only if the kernel
+    sources are unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(call_label)
+    if not e or e.get("kernel_src_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- the workload on the GPU
+def call_label(s) -> str:
+    return (f"B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}_c{int(s.causal)}_w{s.window}")
+
+
+def prepare(workload: str, device):
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    calls = []
+    for shape, cid, layer in ai.workload_calls(workload):
+        q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+        c = {"shape": shape, "q_host": q, "k_host": k, "v_host": v,
+             "q": q.to(device), "k": k.to(device), "v": v.to(device)}
+        c["o"] = torch.empty_like(c["q"])
+        c["lse"] = torch.empty((shape.B, shape.Hq, shape.Nq), device=device, dtype=torch.float32)
+        c["dtype_code"] = attn.ATTN_DTYPE_BF16 if shape.dtype == "bf16" else attn.ATTN_DTYPE_FP16
+        c["flops"] = acc.shape_flops(shape)
+        c["bytes"] = acc.shape_bytes(shape)
+        c["label"] = call_label(shape)
+        calls.append(c)
+    return calls
+
+
+def launch(c, stream_handle):
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    s = c["shape"]
+    st = attn.attn_fwd_ex(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["o"].data_ptr(),
+                          c["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale,
+                          c["dtype_code"], None, 0, stream_handle)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"attn_fwd_ex failed: {attn.attn_status_string(st)}")
+
+
+def make_event():
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+def build_graph(calls, stream):
+    """Capture one step (every call, with a timing event between launches)."""
+    evs = [make_event() for _ in range(len(calls) + 1)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        # warm the launch path (tensor-map encoder, kernel attributes) before capture
+        for c in calls:
+            launch(c, stream.cuda_stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            evs[0].record(stream)
+            for i, c in enumerate(calls):
+                launch(c, stream.cuda_stream)
+                evs[i + 1].record(stream)
+    return g, evs
+
+
+def device_timing(calls, steps, warmup, device, stream):
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    g, evs = build_graph(calls, stream)
+    t_start, t_stop = make_event(), make_event()
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        g.replay()
+    torch.cuda.synchronize(device)
+    step_ms, call_ms = [], [[] for _ in calls]
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(0.0)
+            t_start.record(stream)
+            g.replay()
+            t_stop.record(stream)
+        stream.synchronize()
+        step_ms.append(t_start.elapsed_time(t_stop))
+        for i in range(len(calls)):
+            call_ms[i].append(evs[i].elapsed_time(evs[i + 1]))
+    st = attn.attn_device_status(stream.cuda_stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel status after timing: {attn.attn_status_string(st)}")
+    return step_ms, call_ms
+
+
+def e2e_timing(calls, steps, warmup, device, stream):
+    """Same metric through the public C entry on HOST buffers: every step copies
+    each call's Q, K, V from pinned host memory, runs, and copies O and LSE
+    back."""
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    pinned = []
+    need = 0
+    for c in calls:
+        s = c["shape"]
+        ph = {k: c[k + "_host"].pin_memory() for k in ("q", "k", "v")}
+        ph["o"] = torch.empty_like(ph["q"]).pin_memory()
+        ph["lse"] = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32).pin_memory()
+        pinned.append(ph)
+        need = max(need, attn.attn_fwd_host_staging_bytes(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, 1))
+    buf = torch.empty(need + 256, dtype=torch.uint8, device=device)
+    base = (buf.data_ptr() + 255) & ~255
+    h2d = d2h = 0
+    for c in calls:
+        s = c["shape"]
+        h2d += (c["q"].numel() + c["k"].numel() + c["v"].numel()) * 2
+        d2h += c["o"].numel() * 2 + s.B * s.Hq * s.Nq * 4
+
+    def one_step():
+        for c, ph in zip(calls, pinned):
+            s = c["shape"]
+            st = attn.attn_fwd_host(ph["q"].data_ptr(), ph["k"].data_ptr(), ph["v"].data_ptr(), ph["o"].data_ptr(),
+                                    ph["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window,
+                                    s.scale, c["dtype_code"], base, need, stream.cuda_stream)
+            if st != attn.ATTN_OK:
+                raise RuntimeError(f"attn_fwd_host failed: {attn.attn_status_string(st)}")
+
+    for _ in range(warmup):
+        one_step()
+    stream.synchronize()
+    t0, t1 = make_event(), make_event()
+    t0.record(stream)
+    for _ in range(steps):
+        one_step()
+    t1.record(stream)
+    stream.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    # result check on the last step: the copied-back O equals the device path's O
+    for c, ph in zip(calls, pinned):
+        if not torch.equal(ph["o"], c["o"].cpu()):
+            raise RuntimeError("host-buffer path disagrees with the device path")
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+def oracle_sample(workload: str, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on a bounded, seeded sample of the workload's
+    query rows (every call contributes).  Returns (flops_done, seconds, cores,
+    description)."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.max_threads()
+    calls = ai.workload_calls(workload)
+    rng = np.random.default_rng(seed)
+    prepared = []
+    for shape, cid, layer in calls:
+        q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+        prepared.append((shape, q.reshape(-1, shape.d), k.to(torch.float64), v.to(torch.float64)))
+
+    def run(rows_per_call):
+        flops = 0.0
+        t = 0.0
+        for shape, qf, kf, vf in prepared:
+            total = shape.B * shape.Hq * shape.Nq
+            n = min(total, rows_per_call)
+            ids = np.sort(rng.choice(total, size=n, replace=False)).astype(np.int64)
+            i = ids % shape.Nq
+            pos = shape.Nk - shape.Nq + i
+            if shape.causal:
+                live = np.minimum(pos + 1, shape.window if shape.window > 0 else pos + 1)
+            else:
+                live = np.full_like(i, shape.Nk)
+            flops += 4.0 * shape.d * float(live.sum())
+            qr = qf[torch.from_numpy(ids)]
+            t0 = time.perf_counter()
+            oracle.attention_rows(qr, ids, kf, vf, B=shape.B, Hq=shape.Hq, Nq=shape.Nq, causal=shape.causal,
+                                  window=shape.window, sm_scale=shape.scale)
+            t += time.perf_counter() - t0
+        return flops, t
+
+    rows = 16
+    f, t = run(rows)
+    while t < budget_s / 8 and rows < 1 << 22:
+        rows *= 4
+        f, t = run(rows)
+    if t < budget_s / 2:
+        scale = max(1.0, (budget_s * 0.75) / max(t, 1e-6))
+        rows = int(rows * scale)
+        f, t = run(rows)
+    desc = (f"{rows} seeded random query rows per call of every call in {workload} "
+            f"(capped at the call's rows), fp64 oracle on {cores} OpenMP threads; work = 4*d per live pair")
+    return f, t, cores, desc
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cid = ai.workload_calls(args.workload)
+    per_step_budget = max(0.5, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, per_step_budget / 4)
+    flops = secs = 0.0
+    cores, desc = 0, ""
+    for k in range(args.steps):
+        f, t, cores, desc = oracle_sample(args.workload, per_step_budget, seed=k + 1)
+        flops += f
+        secs += t
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                   "sample": "bounded row sample per step (oracle is row-independent)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    ws, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(ws, "nccl")
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    attn.lib()
+    peaks, peaks_src = load_peaks()
+    calls = prepare(args.workload, device)
+    stream = torch.cuda.Stream(device)
+    steps, warmup = args.steps, max(3, args.warmup)
+
+    dist_barrier(ws)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    step_ms, call_ms = device_timing(calls, steps, warmup, device, stream)
+    clocks = sampler.stop()
+    torch.cuda.synchronize(device)
+    dist_barrier(ws)
+
+    total_ms = dist_max(ws, float(sum(step_ms)), device)
+    flops_step = sum(c["flops"] for c in calls)
+    value = ws * flops_step * steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / steps
+
+    # dominant kernel: the call with the largest share of device time
+    avg = [float(np.mean(m)) for m in call_ms]
+    dom = int(np.argmax(avg))
+    dc = calls[dom]
+    s = dc["shape"]
+    ai_flop_per_byte = dc["flops"] / dc["bytes"]
+    peak_t = peaks["bf16_tflops"]
+    ridge = peak_t * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai_flop_per_byte >= ridge:
+        achieved = dc["flops"] / (avg[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": achieved / peak_t}
+    else:
+        achieved = dc["bytes"] / (avg[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof["traffic"] = profiled_traffic(args.workload, dc["label"])
+    roof["kernel"] = f"attn_fwd_kernel<{s.d},{'bf16' if s.dtype == 'bf16' else 'fp16'}> {dc['label']}"
+    roof["algorithmic"] = {"flops": dc["flops"], "bytes": dc["bytes"]}
+    roof["peak_source"] = f"{peaks_src} (burst bf16 dense; fp16 same rate)" if roof["bound"] == "tensor" \
+        else f"{peaks_src} HBM copy"
+    roof["launch_ms"] = avg[dom]
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_timing(calls, max(3, steps // 4), 2, device, stream)
+        e2e_ms = dist_max(ws, e2e_ms, device)
+        e2e = {"value": ws * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        f, t, cores, desc = oracle_sample(args.workload, args.cpu_seconds)
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": t}
+
+    if args.per_call and rank == 0:
+        for c, a in zip(calls, avg):
+            print(f"{c['label']}: {a * 1e3:.1f} us  {c['flops'] / (a * 1e-3) / 1e12:.1f} TFLOP/s  "
+                  f"{c['bytes'] / (a * 1e-3) / 1e9:.0f} GB/s", file=sys.stderr)
+
+    if rank == 0:
+        line = {
+            "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": steps,
+            "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": calls[0]["shape"].dtype, "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                       "calls_per_step": len(calls),
+                       "flop_convention": "4*B*Hq*N^2*d, halved for square causal; exact live pairs otherwise",
+                       "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                       "launch": "one CUDA graph per step", "parallelism": f"replicas x{ws}"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": steps * len(calls), "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,124 @@
+/*
+ * attn.h -- C ABI of libattn: the tiled (FlashAttention) forward pass on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (lynx-cortex phase-27 lab 02 "Forward de flash attention en
+ * Triton", kernel skeleton and "Bloque C"; cruxr.ai "Optimizaciones de
+ * Atencion", section "FlashAttention: Nunca materializar la matriz de
+ * atencion"): for every batch b, query head h and query row i,
+ *
+ *   O[b,h,i,:] = sum_j softmax_j(sm_scale * Q[b,h,i,:] . K[b,kvh,j,:] + mask) V[b,kvh,j,:]
+ *   LSE[b,h,i] = ln sum_j exp(sm_scale * Q[b,h,i,:] . K[b,kvh,j,:] + mask)
+ *
+ * computed tile by tile with the online-softmax recurrence so that the score
+ * matrix never reaches device memory.
+ *   - GQA/MQA: Hq query heads share Hkv K/V heads, kvh = h / (Hq / Hkv)
+ *     (consecutive groups; cruxr.ai "Multi-Head Latent Attention" recap of
+ *     GQA and the motivation page's "Grouped/Multi-Query Attention").
+ *   - causal: key j is visible to query i iff j <= Nk - Nq + i (the square
+ *     case Nq == Nk keeps j <= i, "position i attends to itself", lab 02
+ *     "Errores tipicos"; for Nq < Nk the queries are the last Nq positions).
+ *   - window > 0 (requires causal): additionally Nk - Nq + i - j < window,
+ *     i.e. the last `window` tokens including itself (motivation page,
+ *     "Sliding window attention").
+ *   - LSE is the natural-log log-sum-exp of the scaled, masked scores (the
+ *     lab 02 skeleton stores m + log(l)).
+ *
+ * Layout: Q, O are (B, Hq, Nq, d) and K, V are (B, Hkv, Nk, d), dense
+ * row-major (d fastest), elements fp16 or bf16; LSE is (B, Hq, Nq) fp32.
+ * All pointers are DEVICE pointers on the current device, 16-byte aligned,
+ * except where a function says HOST.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * memory on any call, never synchronises, and only enqueues work on `stream`;
+ * results are complete when the stream reaches that point.  O and LSE are
+ * fully overwritten; LSE may be NULL (then it is not written).  Q, K, V are
+ * read only.  Outputs must not alias inputs.
+ *
+ * Errors: every call validates its arguments on the host and returns a status
+ * without launching anything when they are bad.  No C++ exception crosses the
+ * ABI.  Launch failures return ATTN_ERR_CUDA.  Kernels bound every internal
+ * wait; a wait that runs out records ATTN_ERR_TIMEOUT in a per-device status
+ * word that attn_device_status() reads back.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, size <= 0, Hq % Hkv != 0,
+                               window < 0, window > 0 without causal, causal with
+                               Nq > Nk, sm_scale not finite or <= 0, bad dtype,
+                               workspace too small */
+  ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or no sm_100-family GPU */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded internal wait ran out */
+} attn_status_t;
+
+typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
+
+/* Square attention, Nq = Nk = N.  Equivalent to attn_fwd_ex with Nq = Nk = N
+ * and no workspace. */
+attn_status_t attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
+                       int Hkv, int N, int d, int causal, int window, float sm_scale, attn_dtype_t dtype,
+                       cudaStream_t stream);
+
+/* General call with Nq query rows against Nk keys (Nq <= Nk when causal; a
+ * decode step is Nq = 1 against an Nk-token cache).
+ *
+ * workspace/workspace_bytes: optional DEVICE scratch for the split-KV path
+ * (cruxr.ai "FlashDecoding": the keys are split into chunks processed in
+ * parallel, each yielding a partial max, sum and output, which a second step
+ * combines by rescaling with exp(m_p - m)).  When workspace is NULL the
+ * non-split path runs.  When it is given it must hold at least
+ * attn_fwd_workspace_bytes(...) bytes, 16-byte aligned, and must not be used
+ * by another call that overlaps on the GPU. */
+attn_status_t attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
+                          int Hkv, int Nq, int Nk, int d, int causal, int window, float sm_scale,
+                          attn_dtype_t dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Scratch bytes the split-KV path wants for this shape (0 when it would not
+ * split). */
+size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+
+/* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
+ * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
+ * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.
+ * dev_buf must hold attn_fwd_host_staging_bytes(...) bytes (256-byte aligned).
+ * The host buffers must stay valid until the stream reaches the end of the
+ * call. */
+attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
+                            float *LSE_host, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                            int window, float sm_scale, attn_dtype_t dtype, void *dev_buf, size_t dev_buf_bytes,
+                            cudaStream_t stream);
+size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_lse);
+
+/* Synchronises `stream`, then reads and clears the current device's kernel
+ * status word: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up a wait since
+ * the last call.  Returns ATTN_ERR_CUDA if the synchronisation fails. */
+attn_status_t attn_device_status(cudaStream_t stream);
+
+/* Test hook: sets the bound, in nanoseconds, on every internal kernel wait of
+ * later launches on any device (default 2e9).  0 restores the default. */
+void attn_set_wait_timeout_ns(unsigned long long ns);
+
+/* Static description of a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/* ATTN_ABI_VERSION of the loaded library. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

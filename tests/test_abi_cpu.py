@@ -1,0 +1,89 @@
+"""The C-ABI library builds, loads and exports every symbol include/attn.h
+declares; host-side validation answers without touching a GPU."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import tiled_attention_forward_fwd_gb300 as m
+
+    m.lib()
+    return m
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_header_symbols_exported(attn):
+    names = declared_functions()
+    assert len(names) >= 9, names
+    L = attn.lib()
+    for n in names:
+        assert hasattr(L, n), f"libattn.so does not export {n}"
+    assert sorted(attn.EXPORTED) == names
+
+
+def test_abi_version_and_strings(attn):
+    assert attn.attn_abi_version() == 1
+    for code, text in [(0, "ok"), (1, "invalid argument"), (3, "CUDA error"), (4, "kernel wait timed out")]:
+        assert attn.attn_status_string(code) == text
+    assert attn.attn_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(B=1, Hq=3, Hkv=2), 1),             # Hq % Hkv
+    (dict(B=0), 1),                            # empty batch
+    (dict(N=0), 1),
+    (dict(d=96), 2),                           # unsupported head dim
+    (dict(window=-1), 1),
+    (dict(window=16, causal=0), 1),            # window needs causal
+    (dict(sm_scale=0.0), 1),
+    (dict(sm_scale=float("inf")), 1),
+    (dict(sm_scale=float("nan")), 1),
+    (dict(dtype=7), 1),
+])
+def test_host_validation(attn, args, expect):
+    a = dict(B=1, Hq=2, Hkv=2, N=64, d=64, causal=1, window=0, sm_scale=0.125, dtype=0)
+    a.update(args)
+    st = attn.attn_fwd(FAKE, FAKE, FAKE, FAKE, None, a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["causal"],
+                       a["window"], a["sm_scale"], a["dtype"], None)
+    assert st == expect
+
+
+def test_null_and_misaligned_pointers(attn):
+    assert attn.attn_fwd(None, FAKE, FAKE, FAKE, None, 1, 2, 2, 64, 64, 0, 0, 0.1, 0, None) == 1
+    assert attn.attn_fwd(FAKE + 8, FAKE, FAKE, FAKE, None, 1, 2, 2, 64, 64, 0, 0, 0.1, 0, None) == 1
+    assert attn.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE + 2, 1, 2, 2, 64, 64, 0, 0, 0.1, 0, None) == 1
+    # causal with more queries than keys
+    assert attn.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 65, 64, 64, 1, 0, 0.1, 0, None, 0, None) == 1
+    # host entry: null host buffer, unaligned staging buffer, staging too small
+    assert attn.attn_fwd_host(None, FAKE, FAKE, FAKE, None, 1, 2, 2, 64, 64, 64, 0, 0, 0.1, 0, FAKE, 1 << 30,
+                              None) == 1
+    assert attn.attn_fwd_host(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 64, 64, 64, 0, 0, 0.1, 0, FAKE + 16, 1 << 30,
+                              None) == 1
+    assert attn.attn_fwd_host(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 64, 64, 64, 0, 0, 0.1, 0, FAKE, 100,
+                              None) == 1
+
+
+def test_sizes(attn):
+    # staging = Q + K + V + O (+ LSE), each rounded up to 256 bytes
+    q = 1 * 2 * 64 * 64 * 2
+    assert attn.attn_fwd_host_staging_bytes(1, 2, 2, 64, 64, 64, 0) == 4 * q
+    assert attn.attn_fwd_host_staging_bytes(1, 2, 2, 64, 64, 64, 1) == 4 * q + 512
+    assert attn.attn_fwd_host_staging_bytes(0, 2, 2, 64, 64, 64, 1) == 0
+    assert attn.attn_fwd_workspace_bytes(1, 2, 3, 1, 64, 64) == 0  # Hq % Hkv

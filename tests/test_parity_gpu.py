@@ -1,0 +1,161 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle
+on the same seeded inputs, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as ai
+from tests import parity_util as pu
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import tiled_attention_forward_fwd_gb300 as m
+
+    m.lib()
+    return m
+
+
+def _run_and_check(shape, oracle_mod, config_id=50, layer=0, label=""):
+    q, k, v = ai.make_qkv(shape, config_id=config_id, layer=layer)
+    o, lse = pu.run_cuda(shape, q, k, v)
+    return pu.check_full(shape, q, k, v, o, lse, oracle_mod, label or str(shape))
+
+
+# ------------------------------------------------------------------ the stated workloads (small ones in full)
+@pytest.mark.parametrize("idx", [0, 1])
+def test_mha_n64(attn, oracle_mod, idx):
+    shape, cid, layer = ai.workload_calls("mha_n64")[idx]
+    _run_and_check(shape, oracle_mod, cid, layer)
+
+
+@pytest.mark.parametrize("idx", range(6))
+def test_mha_b2h4(attn, oracle_mod, idx):
+    shape, cid, layer = ai.workload_calls("mha_b2h4")[idx]
+    _run_and_check(shape, oracle_mod, cid, layer)
+
+
+# ------------------------------------------------------------------ ragged and tiny shapes
+@pytest.mark.parametrize("N", [1, 2, 15, 16, 17, 63, 65, 127, 128, 129, 255, 257, 300])
+@pytest.mark.parametrize("d,dtype", [(64, "fp16"), (64, "bf16"), (128, "fp16"), (128, "bf16")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged(attn, oracle_mod, N, d, dtype, causal):
+    shape = ai.AttnShape(1, 2, 1, N, N, d, dtype, causal)
+    _run_and_check(shape, oracle_mod, 51, N)
+
+
+@pytest.mark.parametrize("Hkv", [1, 2, 4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_gqa_groups(attn, oracle_mod, Hkv, d):
+    shape = ai.AttnShape(2, 8, Hkv, 300, 300, d, "bf16", True)
+    _run_and_check(shape, oracle_mod, 52, Hkv)
+
+
+@pytest.mark.parametrize("window", [1, 2, 37, 127, 128, 129, 300, 699, 700, 5000])
+@pytest.mark.parametrize("d,dtype", [(64, "fp16"), (128, "bf16")])
+def test_sliding_window(attn, oracle_mod, window, d, dtype):
+    shape = ai.AttnShape(1, 4, 2, 700, 700, d, dtype, True, window)
+    _run_and_check(shape, oracle_mod, 53, window)
+
+
+@pytest.mark.parametrize("Nq", [1, 5, 128, 130, 300, 777])
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 200)])
+def test_queries_fewer_than_keys(attn, oracle_mod, Nq, causal, window):
+    """Nq < Nk: bottom-right causal alignment (the queries are the last Nq
+    positions); decode is Nq = 1."""
+    shape = ai.AttnShape(2, 4, 2, Nq, 777, 128, "fp16", causal, window)
+    _run_and_check(shape, oracle_mod, 54, Nq)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("key_scale", [3.0, 8.0])
+def test_rescale_stress(attn, oracle_mod, d, key_scale):
+    """Scores that grow along the key axis, so the running row maximum rises on
+    every K/V tile (exercising the lazy rescale of O), with large magnitudes:
+    every query is a fixed direction u plus noise, key j is
+    key_scale * (j / N) * u plus noise."""
+    N = 1000
+    shape = ai.AttnShape(1, 2, 2, N, N, d, "fp16", False)
+    u = ai.normal_tensor(80 + d, (d,), "f64")
+    noise_q = ai.normal_tensor(81, (1, 2, N, d), "f64") * 0.1
+    noise_k = ai.normal_tensor(82, (1, 2, N, d), "f64")
+    ramp = torch.arange(N, dtype=torch.float64)[None, None, :, None] / N
+    q = (u + noise_q).to(torch.float16)
+    k = (key_scale * ramp * u + noise_k).to(torch.float16)
+    v = ai.normal_tensor(83, (1, 2, N, d), "fp16")
+    o, lse = pu.run_cuda(shape, q, k, v)
+    pu.check_full(shape, q, k, v, o, lse, oracle_mod, "rescale stress")
+
+
+def test_lse_optional_and_streams(attn, oracle_mod):
+    shape = ai.AttnShape(2, 4, 4, 333, 333, 64, "fp16", True)
+    q, k, v = ai.make_qkv(shape, config_id=56)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = pu.run_cuda(shape, q, k, v, with_lse=False)
+    s.synchronize()
+    assert lse is None
+    o_ref, _ = oracle_mod.attention(q, k, v, causal=True)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= pu.TOL_O["fp16"]
+
+
+def test_outputs_fully_overwritten(attn, oracle_mod):
+    shape = ai.AttnShape(1, 2, 2, 130, 130, 64, "fp16", False)
+    q, k, v = ai.make_qkv(shape, config_id=57)
+    out = torch.full((1, 2, 130, 64), float("nan"), device="cuda", dtype=torch.float16)
+    lse = torch.full((1, 2, 130), float("nan"), device="cuda")
+    attn.flash_attn_forward(q.cuda(), k.cuda(), v.cuda(), out=out, lse=lse)
+    assert attn.device_status() == attn.ATTN_OK
+    pu.check_full(shape, q, k, v, out, lse, oracle_mod)
+
+
+def test_bad_arguments_return_status(attn):
+    q = torch.zeros(1, 3, 64, 64, device="cuda", dtype=torch.float16)
+    k = torch.zeros(1, 2, 64, 64, device="cuda", dtype=torch.float16)
+    with pytest.raises(attn.AttnError) as e:
+        attn.flash_attn_forward(q, k, k)  # Hq % Hkv != 0
+    assert e.value.status == attn.ATTN_ERR_INVALID_ARG
+    q2 = torch.zeros(1, 2, 64, 96, device="cuda", dtype=torch.float16)
+    with pytest.raises(attn.AttnError) as e:
+        attn.flash_attn_forward(q2, q2, q2)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+    q3 = torch.zeros(1, 2, 65, 64, device="cuda", dtype=torch.float16)
+    kv = torch.zeros(1, 2, 64, 64, device="cuda", dtype=torch.float16)
+    with pytest.raises(attn.AttnError) as e:
+        attn.flash_attn_forward(q3, kv, kv, causal=True)  # causal with Nq > Nk
+    assert e.value.status == attn.ATTN_ERR_INVALID_ARG
+    with pytest.raises(attn.AttnError) as e:
+        attn.flash_attn_forward(kv, kv, kv, causal=False, window=8)
+    assert e.value.status == attn.ATTN_ERR_INVALID_ARG
+    assert attn.device_status() == attn.ATTN_OK
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled rows
+@pytest.mark.parametrize("layer", [0, 11])
+def test_gpt_stack_full_size(attn, oracle_mod, layer):
+    shape, cid, _ = ai.workload_calls("gpt_stack")[layer]
+    q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+    o, lse = pu.run_cuda(shape, q, k, v)
+    pu.check_properties(shape, v, o, lse)
+    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=512, seed=layer, label=f"gpt layer {layer}")
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_gqa_mqa_full_size(attn, oracle_mod, idx):
+    shape, cid, layer = ai.workload_calls("gqa_mqa")[idx]
+    q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+    o, lse = pu.run_cuda(shape, q, k, v)
+    pu.check_properties(shape, v, o, lse)
+    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=512, seed=idx, label=f"gqa_mqa {idx}")
+
+
+def test_long_prefill_full_size(attn, oracle_mod):
+    shape, cid, layer = ai.workload_calls("long_prefill")[0]
+    q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+    o, lse = pu.run_cuda(shape, q, k, v)
+    pu.check_properties(shape, v, o, lse)
+    stats = pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=768, seed=4, label="long prefill")
+    print("long_prefill", stats)

@@ -1,0 +1,178 @@
+"""Tiled (FlashAttention) forward pass for NVIDIA GB300 (sm_103a).
+
+Thin ctypes binding over ``libattn.so`` (C ABI in ``include/attn.h``).  The
+functions below keep the C names and only marshal arguments; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library cannot be built or loaded, importing this package raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+
+ATTN_DTYPE_FP16 = 0
+ATTN_DTYPE_BF16 = 1
+
+EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
+            "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {attn_status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if needed) libattn.so.  Raises if unavailable."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        fp = ctypes.POINTER(ctypes.c_float)
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        L.attn_fwd.restype = ci
+        L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp, sz, vp]
+        L.attn_fwd_ex.restype = ci
+        L.attn_fwd_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
+        L.attn_fwd_workspace_bytes.restype = sz
+        L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp, sz, vp]
+        L.attn_fwd_host.restype = ci
+        L.attn_fwd_host_staging_bytes.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+        L.attn_fwd_host_staging_bytes.restype = sz
+        L.attn_device_status.argtypes = [vp]
+        L.attn_device_status.restype = ci
+        L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        L.attn_set_wait_timeout_ns.restype = None
+        L.attn_status_string.argtypes = [ci]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_abi_version.argtypes = []
+        L.attn_abi_version.restype = ci
+        del fp
+        _lib = L
+        return _lib
+
+
+# ------------------------------------------------------------------ raw C names
+def attn_fwd(Q, K, V, O, LSE, B, Hq, Hkv, N, d, causal, window, sm_scale, dtype, stream) -> int:
+    return lib().attn_fwd(Q, K, V, O, LSE, B, Hq, Hkv, N, d, int(causal), int(window), float(sm_scale), int(dtype),
+                          stream)
+
+
+def attn_fwd_ex(Q, K, V, O, LSE, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, workspace,
+                workspace_bytes, stream) -> int:
+    return lib().attn_fwd_ex(Q, K, V, O, LSE, B, Hq, Hkv, Nq, Nk, d, int(causal), int(window), float(sm_scale),
+                             int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
+    return int(lib().attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d))
+
+
+def attn_fwd_host(Qh, Kh, Vh, Oh, LSEh, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, dev_buf,
+                  dev_buf_bytes, stream) -> int:
+    return lib().attn_fwd_host(Qh, Kh, Vh, Oh, LSEh, B, Hq, Hkv, Nq, Nk, d, int(causal), int(window),
+                               float(sm_scale), int(dtype), dev_buf, int(dev_buf_bytes), stream)
+
+
+def attn_fwd_host_staging_bytes(B, Hq, Hkv, Nq, Nk, d, with_lse) -> int:
+    return int(lib().attn_fwd_host_staging_bytes(B, Hq, Hkv, Nq, Nk, d, int(bool(with_lse))))
+
+
+def attn_device_status(stream) -> int:
+    return int(lib().attn_device_status(stream))
+
+
+def attn_set_wait_timeout_ns(ns: int) -> None:
+    lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def attn_abi_version() -> int:
+    return int(lib().attn_abi_version())
+
+
+# ------------------------------------------------------------------ torch-facing
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return ATTN_DTYPE_FP16
+    if t.dtype == torch.bfloat16:
+        return ATTN_DTYPE_BF16
+    raise TypeError(f"attention inputs must be float16 or bfloat16, got {t.dtype}")
+
+
+def _stream_handle(device) -> int:
+    torch = _torch()
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def flash_attn_forward(q, k, v, causal: bool = False, window: int = 0, sm_scale: float | None = None,
+                       return_lse: bool = True, out=None, lse=None, workspace=None):
+    """O = softmax(sm_scale * q k^T + mask) v on CUDA tensors.
+
+    q: (B, Hq, Nq, d); k, v: (B, Hkv, Nk, d); fp16 or bf16, same dtype and
+    device.  ``sm_scale`` defaults to 1/sqrt(d).  Returns ``(O, LSE)`` (LSE is
+    fp32 (B, Hq, Nq), or None when ``return_lse`` is False).  ``workspace`` (a
+    CUDA byte tensor of ``attn_fwd_workspace_bytes`` bytes) enables the
+    split-KV path for small query counts.  Runs on the current stream."""
+    torch = _torch()
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("flash_attn_forward needs CUDA tensors (no CPU path)")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be (B,Hq,Nq,d) and k, v (B,Hkv,Nk,d)")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k, v batch / head dim do not match q")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                     lse.data_ptr() if return_lse else None, B, Hq, Hkv, Nq, Nk, d, causal, window, scale,
+                     _dtype_code(q), ws_ptr, ws_bytes, _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_ex")
+    return out, (lse if return_lse else None)
+
+
+def device_status(device=None) -> int:
+    """Synchronise the current stream and read/clear the kernel status word."""
+    return attn_device_status(_stream_handle(device))
+
+
+__all__ = EXPORTED + ["flash_attn_forward", "device_status", "lib", "AttnError"]

@@ -1,0 +1,253 @@
+// attn_api.cu -- the C ABI declared in include/attn.h: argument checks,
+// TMA tensor maps, kernel selection and launch.  No allocation, no sync
+// (except attn_device_status, whose job is to sync).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_decode.cuh"
+#include "attn_fwd_sm103.cuh"
+
+namespace attn {
+
+// Kernel status word (one per device): first error code wins, 0 = fine.
+__device__ int g_status;
+
+static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D view (d, rows, slabs) of a dense (slabs, rows, d) 16-bit tensor, box
+// 64 x 128 x 1 with 128-byte swizzle.  Rows past `rows` read as zero and are
+// never written by stores.
+static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long slabs, bool bf16) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slabs)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * rows};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Shape {
+  int B, Hq, Hkv, Nq, Nk, d, causal, window;
+  float sm_scale;
+  attn_dtype_t dtype;
+};
+
+static attn_status_t validate(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                              const Shape &s) {
+  if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return ATTN_ERR_INVALID_ARG;
+  if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (s.B <= 0 || s.Hq <= 0 || s.Hkv <= 0 || s.Nq <= 0 || s.Nk <= 0 || s.d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (s.Hq % s.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (s.window < 0 || (s.window > 0 && !s.causal)) return ATTN_ERR_INVALID_ARG;
+  if (s.causal && s.Nq > s.Nk) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(s.sm_scale) || !(s.sm_scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (s.dtype != ATTN_DTYPE_FP16 && s.dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+  if (s.d != 64 && s.d != 128) return ATTN_ERR_UNSUPPORTED;
+  // grid limits of the prefill launch: x = B*Hq, y = ceil(Nq/128)
+  if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if ((s.Nq + kBM - 1) / kBM > 65535) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+static int current_device_sm_major(int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int major = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
+  if (dev_out) *dev_out = dev;
+  return major;
+}
+
+template <int D, bool BF16>
+static attn_status_t launch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                   const Shape &s, cudaStream_t stream) {
+  using Cfg = FwdCfg<D>;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long zq = static_cast<long long>(s.B) * s.Hq;
+  const long long zk = static_cast<long long>(s.B) * s.Hkv;
+  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16) ||
+      !make_map(&p.tmV, V, D, s.Nk, zk, BF16) || !make_map(&p.tmO, O, D, s.Nq, zq, BF16))
+    return ATTN_ERR_CUDA;
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  p.lse = LSE;
+  p.status = status;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Nq = s.Nq;
+  p.Nk = s.Nk;
+  p.group = s.Hq / s.Hkv;
+  p.causal = s.causal ? 1 : 0;
+  p.window = s.window;
+  p.num_q_tiles = (s.Nq + kBM - 1) / kBM;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  p.timeout_ns = g_timeout_ns.load();
+
+  auto kern = attn_fwd_kernel<D, BF16>;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(attr_once[dev & 63], [&] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  });
+  dim3 grid(static_cast<unsigned>(zq), static_cast<unsigned>(p.num_q_tiles));
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                      const Shape &s, cudaStream_t stream) {
+  const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
+  if (s.d == 64) return bf16 ? launch_prefill<64, true>(Q, K, V, O, LSE, s, stream)
+                             : launch_prefill<64, false>(Q, K, V, O, LSE, s, stream);
+  return bf16 ? launch_prefill<128, true>(Q, K, V, O, LSE, s, stream)
+              : launch_prefill<128, false>(Q, K, V, O, LSE, s, stream);
+}
+
+static attn_status_t run(const void *Q, const void *K, const void *V, void *O, float *LSE, const Shape &s,
+                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+  attn_status_t st = validate(Q, K, V, O, LSE, s);
+  if (st != ATTN_OK) return st;
+  if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  if (ws != nullptr) {
+    const size_t need = decode_workspace_bytes(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d);
+    if (need > 0) {
+      if (ws_bytes < need || !aligned16(ws)) return ATTN_ERR_INVALID_ARG;
+      int *status = nullptr;
+      if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+      return launch_decode(Q, K, V, O, LSE, s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.sm_scale,
+                           s.dtype == ATTN_DTYPE_BF16, ws, status, stream)
+                 ? ATTN_OK
+                 : ATTN_ERR_CUDA;
+    }
+  }
+  return dispatch_prefill(Q, K, V, O, LSE, s, stream);
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq, int Hkv,
+                       int N, int d, int causal, int window, float sm_scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+  Shape s{B, Hq, Hkv, N, N, d, causal, window, sm_scale, dtype};
+  return run(Q, K, V, O, LSE, s, nullptr, 0, stream);
+}
+
+attn_status_t attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
+                          int Hkv, int Nq, int Nk, int d, int causal, int window, float sm_scale,
+                          attn_dtype_t dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Shape s{B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype};
+  return run(Q, K, V, O, LSE, s, workspace, workspace_bytes, stream);
+}
+
+size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128) || Hq % Hkv) return 0;
+  return decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+}
+
+static size_t round_up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_lse) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return 0;
+  const size_t q = static_cast<size_t>(B) * Hq * Nq * d * 2;
+  const size_t kv = static_cast<size_t>(B) * Hkv * Nk * d * 2;
+  const size_t lse = with_lse ? static_cast<size_t>(B) * Hq * Nq * 4 : 0;
+  return round_up256(q) * 2 + round_up256(kv) * 2 + round_up256(lse);
+}
+
+attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
+                            float *LSE_host, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
+                            float sm_scale, attn_dtype_t dtype, void *dev_buf, size_t dev_buf_bytes,
+                            cudaStream_t stream) {
+  if (!Q_host || !K_host || !V_host || !O_host || !dev_buf) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dev_buf) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
+  Shape s{B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype};
+  const size_t need = attn_fwd_host_staging_bytes(B, Hq, Hkv, Nq, Nk, d, LSE_host != nullptr);
+  if (need == 0 || dev_buf_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const size_t q = static_cast<size_t>(B) * Hq * Nq * d * 2;
+  const size_t kv = static_cast<size_t>(B) * Hkv * Nk * d * 2;
+  uint8_t *base = static_cast<uint8_t *>(dev_buf);
+  void *dQ = base;
+  void *dK = base + round_up256(q);
+  void *dV = base + round_up256(q) + round_up256(kv);
+  void *dO = base + round_up256(q) + 2 * round_up256(kv);
+  float *dL = LSE_host ? reinterpret_cast<float *>(base + 2 * round_up256(q) + 2 * round_up256(kv)) : nullptr;
+  attn_status_t st = validate(dQ, dK, dV, dO, dL, s);
+  if (st != ATTN_OK) return st;
+  if (cudaMemcpyAsync(dQ, Q_host, q, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  st = run(dQ, dK, dV, dO, dL, s, nullptr, 0, stream);
+  if (st != ATTN_OK) return st;
+  if (cudaMemcpyAsync(O_host, dO, q, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dL && cudaMemcpyAsync(LSE_host, dL, static_cast<size_t>(B) * Hq * Nq * 4, cudaMemcpyDeviceToHost, stream) !=
+                cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status_t attn_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+void attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
+
+const char *attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension or device";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+}  // extern "C"
