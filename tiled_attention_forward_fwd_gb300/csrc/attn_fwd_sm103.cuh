@@ -256,7 +256,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
     const int pos = i0 + row + off;  // absolute position of this query row
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
-    float l = 0.f;        // running sum of exp2(s * sl2 - m)
+    float l = 0.f;        // running sum of exp2(s * sl2 - m) in fp32 (gives LSE)
+    float lq = 0.f;       // the same sum over the 16-bit rounded probabilities (normalises O)
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int kt = kv_begin + j;
@@ -306,10 +307,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           tmem_st32(ocol, r);
         }
         l *= alpha;
+        lq *= alpha;
         m = m_new;
       }
       const float mref = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      float rs = 0.f, rsq = 0.f;
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
@@ -318,14 +320,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           const float e0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
           const float e1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
           pk[i] = pack2<BF16>(e0, e1);
-          // l sums the 16-bit probabilities the P V contraction really uses,
-          // so the normalised weights of every row add up to one.
+          rs += e0 + e1;
+          // lq sums the 16-bit probabilities the P V contraction really uses,
+          // so the weights that normalise O add up to one.
           const float2 r2 = unpack2<BF16>(pk[i]);
-          rs += r2.x + r2.y;
+          rsq += r2.x + r2.y;
         }
         tmem_st16(scol + c * 16, pk);
       }
       l += rs;
+      lq += rsq;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
     if (ok) ok = mbar_wait_warp(bOfinal, 0, wc, kErrWaitOFinal);
     if (ok) {
       tc_fence_after();
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv_l = (lq > 0.f) ? 1.f / lq : 0.f;
       uint8_t *stage = smem + C::kOffQ;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
