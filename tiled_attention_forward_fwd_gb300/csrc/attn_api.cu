@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -73,9 +74,8 @@ static attn_status_t validate(const void *Q, const void *K, const void *V, const
   if (!std::isfinite(s.sm_scale) || !(s.sm_scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (s.dtype != ATTN_DTYPE_FP16 && s.dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
   if (s.d != 64 && s.d != 128) return ATTN_ERR_UNSUPPORTED;
-  // grid limits of the prefill launch: x = B*Hq, y = ceil(Nq/128)
-  if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
-  if ((s.Nq + kBM - 1) / kBM > 65535) return ATTN_ERR_INVALID_ARG;
+  // work items are counted in 32-bit integers
+  if (static_cast<long long>(s.B) * s.Hq * ((s.Nq + kBM - 1) / kBM) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -97,10 +97,11 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   const long long zq = static_cast<long long>(s.B) * s.Hq;
   const long long zk = static_cast<long long>(s.B) * s.Hkv;
   if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16) ||
-      !make_map(&p.tmV, V, D, s.Nk, zk, BF16) || !make_map(&p.tmO, O, D, s.Nq, zq, BF16))
+      !make_map(&p.tmV, V, D, s.Nk, zk, BF16))
     return ATTN_ERR_CUDA;
   int *status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  p.O = O;
   p.lse = LSE;
   p.status = status;
   p.B = s.B;
@@ -111,18 +112,35 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.group = s.Hq / s.Hkv;
   p.causal = s.causal ? 1 : 0;
   p.window = s.window;
-  p.num_q_tiles = (s.Nq + kBM - 1) / kBM;
+  // An item holds two query tiles: two heads of one GQA group at the same
+  // rows when the group size is even, else two consecutive row tiles.
+  p.heads_mode = (p.group % 2 == 0) ? 1 : 0;
+  const int rows_per_item = p.heads_mode ? kBM : 2 * kBM;
+  p.n_row_blocks = (s.Nq + rows_per_item - 1) / rows_per_item;
+  const long long slots = p.heads_mode ? zq / 2 : zq;
+  const long long items = slots * p.n_row_blocks;
+  if (items > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  p.n_slots = static_cast<int>(slots);
+  p.n_items = static_cast<int>(items);
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
 
   auto kern = attn_fwd_kernel<D, BF16>;
-  static std::once_flag attr_once[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  std::call_once(attr_once[dev & 63], [&] {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  static int n_sms[64];
+  static bool regs_ok[64];
+  std::call_once(attr_once[dev], [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    cudaDeviceGetAttribute(&n_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    // The warpgroup register split (setmaxnreg) is sized for a launch of
+    // kThreads x kLaunchRegs registers; any other allocation could stall.
+    cudaFuncAttributes fa;
+    regs_ok[dev] = cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs == kLaunchRegs;
   });
-  dim3 grid(static_cast<unsigned>(zq), static_cast<unsigned>(p.num_q_tiles));
+  if (!regs_ok[dev] || n_sms[dev] <= 0) return ATTN_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>(std::min<long long>(items, n_sms[dev]));
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

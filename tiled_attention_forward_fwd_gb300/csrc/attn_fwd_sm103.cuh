@@ -1,25 +1,32 @@
 // attn_fwd_sm103.cuh -- tiled attention forward (prefill) for sm_103a.
 //
-// One CTA computes one 128-row tile of queries of one (batch, query head)
-// against every live 128-key tile of its K/V head: the tiling of the cruxr.ai
-// "FlashAttention" section (outer loop over Q blocks, inner loop over K/V
-// blocks, online softmax, one write of O) and of the lab 02 kernel skeleton
-// (one program per (batch x head, query tile); running max m, running sum l
-// and an fp32 accumulator; O / l and LSE = m + log l stored at the end).
+// The computation is the tiling of the cruxr.ai "FlashAttention" section
+// (outer loop over Q blocks, inner loop over K/V blocks, online softmax with a
+// running max and running sum, one write of O) and of the lab 02 kernel
+// skeleton (running max m, running sum l and an fp32 accumulator per query
+// row; O / l and the log-sum-exp m + log l stored at the end).
 //
-// GB300 mapping (warp-specialised, 6 warps):
-//   warp 0      TMA producer: Q tile once, then K_j / V_j into an NS-stage
-//               shared-memory ring (128B-swizzled boxes of 128 rows x 64 cols)
-//   warp 1      owns TMEM (512 columns) and issues tcgen05.mma from one lane:
-//                 S_j = Q K_j^T      (A, B from shared memory, fp32 in TMEM)
-//                 O  += P_j V_j      (A = P from TMEM, B = V from shared memory)
-//   warps 2..5  softmax + epilogue: thread r owns query row r (TMEM lane r):
-//               loads its S row from TMEM, masks, updates the running max and
-//               sum in the log2 domain (sm_scale folded into log2 e), writes P
-//               as packed 16-bit pairs back over the S columns, rescales O in
-//               TMEM only when the running max grew by more than 2^8, and at
-//               the end writes O / l (TMA store) and LSE.
-// TMEM columns: S/P double buffer at [0,128) and [128,256), O at [256,256+D).
+// GB300 mapping.  A persistent grid (one CTA per SM) walks a static list of
+// work items, longest first.  An item is two 128-row query tiles that read
+// the same K/V rows: two heads of one GQA group at the same rows when the
+// group size is even (each K/V tile load then serves both heads), else two
+// consecutive row tiles of one head.  12 warps in three warpgroups:
+//   WG0  warp 0: TMA producer -- Q tiles, then K_j / V_j into an NS-stage
+//                shared-memory ring (128B-swizzled boxes of 128 rows x 64 cols)
+//        warp 1: owns TMEM (512 columns) and issues tcgen05.mma from one lane:
+//                  S_t = Q_t K_j^T  (A, B in shared memory, fp32 in TMEM)
+//                  O_t += P_t V_j   (A = P_t in TMEM, B = V_j in shared memory)
+//                alternating between the two tiles so that one tile's
+//                contractions run while the other tile's softmax runs
+//   WG1, WG2     softmax of tile 0 / tile 1: thread r owns query row r (TMEM
+//                lane r); loads its S row, masks, keeps the running max and
+//                sums in the log2 domain (sm_scale folded into log2 e), writes
+//                P as packed 16-bit pairs over the S columns, and rescales its
+//                O row in TMEM only when the running max grew by more than 2^8;
+//                after an item's last tile it reads O_t, frees it for the next
+//                item and writes O / l (16-bit) and LSE to global memory
+// TMEM columns: S/P of tile t at [128 t, 128 t + 128), O_t at 256 + t*D.
+// Every mbarrier wait is bounded (see sm103_ptx.cuh).
 #pragma once
 
 #include "sm103_ptx.cuh"
@@ -28,7 +35,7 @@ namespace attn {
 
 constexpr int kBM = 128;  // query rows per tile (tcgen05 M)
 constexpr int kBN = 128;  // keys per K/V tile (MMA N of S, MMA K of P V)
-constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold: factor 256
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold: a factor 256
 
 enum DeviceError : int {
   kErrWaitQ = 0x101,
@@ -36,41 +43,54 @@ enum DeviceError : int {
   kErrWaitKVEmpty = 0x103,
   kErrWaitS = 0x104,
   kErrWaitP = 0x105,
-  kErrWaitO = 0x106,
+  kErrWaitOFree = 0x106,
   kErrWaitOFinal = 0x107,
+  kErrWaitQFree = 0x108,
 };
 
 struct FwdParams {
   CUtensorMap tmQ;  // (d, Nq, B*Hq)
   CUtensorMap tmK;  // (d, Nk, B*Hkv)
   CUtensorMap tmV;  // (d, Nk, B*Hkv)
-  CUtensorMap tmO;  // (d, Nq, B*Hq)
+  void *O;          // (B*Hq*Nq, d) 16-bit
   float *lse;       // (B*Hq*Nq) or null
   int *status;      // device status word
   int B, Hq, Hkv, Nq, Nk, group;
   int causal, window;
-  int num_q_tiles;
+  int heads_mode;    // 1: item = heads (h, h+1) at the same 128 rows; 0: rows (r, r+128) of one head
+  int n_row_blocks;  // row blocks per (b, head slot)
+  int n_slots;       // heads_mode ? B*Hq/2 : B*Hq
+  int n_items;
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
 };
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = (D == 64) ? 4 : 3;
-  static constexpr int kBoxBytes = 128 * 128;  // 128 rows x 64 cols x 2 bytes
-  static constexpr int kTileBytes = kBN * D * 2;
-  static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kStages = (D == 64) ? 4 : 2;  // K/V ring depth
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q buffers per tile (2: next item prefetched)
+  static constexpr int kBoxBytes = 128 * 128;        // 128 rows x 64 cols x 2 bytes
+  static constexpr int kTileBytes = kBN * D * 2;     // one K or V tile
+  static constexpr int kQBytes = kBM * D * 2;        // one Q tile
+  static constexpr int kOffQ = 0;                    // [tile][buf]
+  static constexpr int kOffK = kOffQ + 2 * kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 3;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
+  // barriers: qfull[2][QB], qfree[2][QB], kfull[NS], vfull[NS], kvempty[NS],
+  //           sfull[2], pfull[2], ofinal[2], ofree[2], drain
+  static constexpr int kNumBars = 4 * kQBufs + 3 * kStages + 8 + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
-  static constexpr int kThreads = 192;
-  static_assert(kNumBars * 8 + 16 <= 256, "barrier area");
+  static constexpr int kThreads = 384;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
+
+// Register budget per warpgroup after setmaxnreg.  The kernel is launched
+// with 384 threads x 168 registers = 64512; the split must not exceed that.
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kRegsWG0 = 72, kRegsSoftmax = 216;
+static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= 384 * kLaunchRegs, "register split");
 
 __device__ __forceinline__ bool key_live(int key, int pos, int Nk, int causal, int window) {
   return key < Nk && (!causal || key <= pos) && (window <= 0 || pos - key < window);
@@ -85,10 +105,93 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// S[tmem] = Q K^T for one 128x128 tile: D/16 MMAs of K = 16, issued back to
+// back.  qd / kd describe the first K-slice; slice k starts (k/4) 64-column
+// boxes plus (k%4)*32 bytes further (16-byte units in the descriptor).
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd) {
+  constexpr uint32_t kIdesc = idesc_f16(kBM, kBN, BF16, false, false);
+  constexpr uint64_t kBox = (128 * 128) >> 4;
+  umma_ss_x4(d_tmem, qd, kd, kIdesc, 0u);
+  if constexpr (D == 128) umma_ss_x4(d_tmem, qd + kBox, kd + kBox, kIdesc, 1u);
+}
+
+// O[tmem] (+)= P V for one tile: 8 MMAs of K = 16 keys, back to back.  P is
+// read from TMEM (8 columns of packed pairs per slice); V is MN-major (d
+// contiguous), and 16 keys are two 8-row swizzle atoms, 2048 bytes further
+// per slice.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd, uint32_t accumulate) {
+  constexpr uint32_t kIdesc = idesc_f16(kBM, D, BF16, false, true);
+  umma_ts_x8(o_tmem, p_tmem, vd, kIdesc, accumulate);
+}
+
+// One work item: up to two query tiles and the K/V tiles each one needs.
+struct Item {
+  int b, kvh;
+  int bh[2];    // b * Hq + h of each tile
+  int row0[2];  // first query row of each tile
+  bool valid[2];
+  int beg[2], end[2];  // live K/V tile range of each tile
+  int ubeg, uend;      // union of the valid tiles' ranges
+};
+
+__device__ __forceinline__ void tile_range(const FwdParams &p, int row0, int &beg, int &end) {
+  const int i1 = min(row0 + kBM, p.Nq);
+  const int off = p.Nk - p.Nq;
+  const int p0 = row0 + off, p1 = i1 - 1 + off;
+  const int nkt = (p.Nk + kBN - 1) / kBN;
+  beg = 0;
+  end = nkt;
+  if (p.causal) {
+    end = min(nkt, p1 / kBN + 1);
+    if (p.window > 0) {
+      const int lo = p0 - p.window + 1;
+      beg = lo > 0 ? lo / kBN : 0;
+    }
+  }
+}
+
+__device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
+  Item it;
+  const int rb = p.n_row_blocks - 1 - item / p.n_slots;  // longest (last) row blocks first
+  const int slot = item % p.n_slots;
+  if (p.heads_mode) {
+    const int hp = p.Hq / 2;
+    it.b = slot / hp;
+    const int h0 = (slot % hp) * 2;
+    it.bh[0] = it.b * p.Hq + h0;
+    it.bh[1] = it.bh[0] + 1;
+    it.kvh = h0 / p.group;
+    it.row0[0] = it.row0[1] = rb * kBM;
+  } else {
+    it.b = slot / p.Hq;
+    const int h = slot % p.Hq;
+    it.bh[0] = it.bh[1] = slot;
+    it.kvh = h / p.group;
+    it.row0[0] = rb * 2 * kBM;
+    it.row0[1] = rb * 2 * kBM + kBM;
+  }
+  it.ubeg = 1 << 30;
+  it.uend = 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    it.valid[t] = it.row0[t] < p.Nq;
+    it.beg[t] = it.end[t] = 0;
+    if (it.valid[t]) {
+      tile_range(p, it.row0[t], it.beg[t], it.end[t]);
+      it.ubeg = min(it.ubeg, it.beg[t]);
+      it.uend = max(it.uend, it.end[t]);
+    }
+  }
+  return it;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int NS = C::kStages;
+  constexpr int QB = C::kQBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
@@ -99,57 +202,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   const uint32_t sK = smem_u32(smem + C::kOffK);
   const uint32_t sV = smem_u32(smem + C::kOffV);
   const uint32_t bar0 = smem_u32(bars);
-  // barrier addresses
-  const uint32_t bQ = bar0;
-  auto bKfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bVfull = [&](int s) { return bar0 + 8u * (1 + NS + s); };
-  auto bKVempty = [&](int s) { return bar0 + 8u * (1 + 2 * NS + s); };
-  auto bSfull = [&](int b) { return bar0 + 8u * (1 + 3 * NS + b); };
-  auto bPfull = [&](int b) { return bar0 + 8u * (3 + 3 * NS + b); };
-  const uint32_t bOdone = bar0 + 8u * (5 + 3 * NS);
-  const uint32_t bOfinal = bar0 + 8u * (6 + 3 * NS);
-  const uint32_t bDrain = bar0 + 8u * (7 + 3 * NS);
+  auto bQfull = [&](int t, int q) { return bar0 + 8u * (t * QB + q); };
+  auto bQfree = [&](int t, int q) { return bar0 + 8u * (2 * QB + t * QB + q); };
+  auto bKfull = [&](int s) { return bar0 + 8u * (4 * QB + s); };
+  auto bVfull = [&](int s) { return bar0 + 8u * (4 * QB + NS + s); };
+  auto bKVempty = [&](int s) { return bar0 + 8u * (4 * QB + 2 * NS + s); };
+  const uint32_t bX = bar0 + 8u * (4 * QB + 3 * NS);  // per-tile barriers follow
+  auto bSfull = [&](int t) { return bX + 8u * (0 + t); };
+  auto bPfull = [&](int t) { return bX + 8u * (2 + t); };
+  auto bOfinal = [&](int t) { return bX + 8u * (4 + t); };
+  auto bOfree = [&](int t) { return bX + 8u * (6 + t); };
+  const uint32_t bDrain = bX + 8u * 8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work item
-  const int bh = blockIdx.x;  // b * Hq + h
-  const int b = bh / p.Hq;
-  const int h = bh - b * p.Hq;
-  const int kvh = h / p.group;
-  const int q_tile = p.num_q_tiles - 1 - static_cast<int>(blockIdx.y);  // long causal tiles first
-  const int i0 = q_tile * kBM;
-  const int i1 = min(i0 + kBM, p.Nq);
-  const int off = p.Nk - p.Nq;
-  const int p0 = i0 + off, p1 = i1 - 1 + off;
-  const int nkt = (p.Nk + kBN - 1) / kBN;
-  int kv_end = nkt, kv_begin = 0;
-  if (p.causal) {
-    kv_end = min(nkt, p1 / kBN + 1);
-    if (p.window > 0) {
-      const int lo = p0 - p.window + 1;
-      kv_begin = lo > 0 ? lo / kBN : 0;
-    }
-  }
-  const int n_tiles = kv_end - kv_begin;  // >= 1 (host guarantees Nq <= Nk when causal)
-
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bQ, 1);
+    for (int t = 0; t < 2; ++t) {
+      for (int q = 0; q < QB; ++q) {
+        mbar_init(bQfull(t, q), 1);
+        mbar_init(bQfree(t, q), 1);
+      }
+      mbar_init(bSfull(t), 1);
+      mbar_init(bPfull(t), 4);
+      mbar_init(bOfinal(t), 1);
+      mbar_init(bOfree(t), 4);
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bKfull(s), 1);
       mbar_init(bVfull(s), 1);
       mbar_init(bKVempty(s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bSfull(i), 1);
-      mbar_init(bPfull(i), 4);
-    }
-    mbar_init(bOdone, 1);
-    mbar_init(bOfinal, 1);
     mbar_init(bDrain, 1);
     fence_mbar_init();
   }
@@ -161,214 +246,252 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int wg = warp >> 2;
 
-  if (warp == 0) {
-    // ================================================================ producer
-    if (lane == 0) {
+  if (wg == 0) {
+    regs_dec<kRegsWG0>();
+    if (warp == 0 && lane == 0) {
+      // ============================================================ TMA producer
       tma_prefetch_desc(&p.tmQ);
       tma_prefetch_desc(&p.tmK);
       tma_prefetch_desc(&p.tmV);
-      mbar_arrive_expect_tx(bQ, C::kQBytes);
+      int nq[2] = {0, 0};
+      int ckv = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item(p, item);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * C::kBoxBytes, &p.tmQ, bQ, c * 64, i0, bh);
-      const int zkv = b * p.Hkv + kvh;
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(bKVempty(s), ((j / NS) - 1) & 1, wc, kErrWaitKVEmpty)) break;
-        const int krow = (kv_begin + j) * kBN;
-        mbar_arrive_expect_tx(bKfull(s), C::kTileBytes);
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || !it.valid[t]) continue;
+          const int k = nq[t], q = k % QB;
+          if (k >= QB && !mbar_wait(bQfree(t, q), ((k / QB) - 1) & 1, wc, kErrWaitQFree)) {
+            ok = false;
+            continue;
+          }
+          const uint32_t dst = sQ + (t * QB + q) * C::kQBytes;
+          mbar_arrive_expect_tx(bQfull(t, q), C::kQBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sK + s * C::kTileBytes + c * C::kBoxBytes, &p.tmK, bKfull(s), c * 64, krow, zkv);
-        mbar_arrive_expect_tx(bVfull(s), C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(dst + c * C::kBoxBytes, &p.tmQ, bQfull(t, q), c * 64, it.row0[t], it.bh[t]);
+          nq[t] = k + 1;
+        }
+        const int zkv = it.b * p.Hkv + it.kvh;
+        for (int j = it.ubeg; ok && j < it.uend; ++j) {
+          const int c = ckv, s = c % NS;
+          if (c >= NS && !mbar_wait(bKVempty(s), ((c / NS) - 1) & 1, wc, kErrWaitKVEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bKfull(s), C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sV + s * C::kTileBytes + c * C::kBoxBytes, &p.tmV, bVfull(s), c * 64, krow, zkv);
-        issued = j + 1;
+          for (int cc = 0; cc < D / 64; ++cc)
+            tma_load_3d(sK + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmK, bKfull(s), cc * 64, j * kBN, zkv);
+          mbar_arrive_expect_tx(bVfull(s), C::kTileBytes);
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc)
+            tma_load_3d(sV + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmV, bVfull(s), cc * 64, j * kBN, zkv);
+          ckv = c + 1;
+        }
       }
       // Never leave the CTA with one of our copies still in flight.
-      mbar_drain(bQ, 0);
-      for (int t = max(0, issued - NS); t < issued; ++t) {
-        mbar_drain(bKfull(t % NS), (t / NS) & 1);
-        mbar_drain(bVfull(t % NS), (t / NS) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_f16(kBM, kBN, BF16, false, false);
-      constexpr uint32_t kIdescPV = idesc_f16(kBM, D, BF16, false, true);
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj % NS;
-        if (!mbar_wait(bPfull(jj & 1), (jj >> 1) & 1, wc, kErrWaitP)) return false;
-        if (!mbar_wait(bVfull(s), (jj / NS) & 1, wc, kErrWaitKV)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sV + s * C::kTileBytes;
-        const uint32_t pcol = tmem + (jj & 1) * 128;
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {
-          // V: MN-major (d contiguous); 16 keys = two 8-row swizzle atoms.
-          const uint64_t bdesc = sdesc_sw128(vbase + k * 2048, C::kBoxBytes, 1024);
-          umma_ts(tmem + C::kColO, pcol + k * 8, bdesc, kIdescPV, (jj > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(bKVempty(s));
-        umma_commit(bOdone);
-        return true;
-      };
-      bool ok = mbar_wait(bQ, 0, wc, kErrWaitQ);
-      int j = 0;
-      for (; ok && j < n_tiles; ++j) {
-        const int s = j % NS;
-        if (!mbar_wait(bKfull(s), (j / NS) & 1, wc, kErrWaitKV)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = sK + s * C::kTileBytes;
-        const uint32_t scol = tmem + (j & 1) * 128;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          // Q, K: K-major; 16 elements = 32 bytes inside a 128-byte swizzle row.
-          const uint32_t koff = (k / 4) * C::kBoxBytes + (k % 4) * 32;
-          const uint64_t adesc = sdesc_sw128(sQ + koff, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(kbase + koff, 16, 1024);
-          umma_ss(scol, adesc, bdesc, kIdescQK, k > 0 ? 1u : 0u);
-        }
-        umma_commit(bSfull(j & 1));
-        if (j > 0 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
-        }
+      for (int t = 0; t < 2; ++t)
+        for (int k = max(0, nq[t] - QB); k < nq[t]; ++k) mbar_drain(bQfull(t, k % QB), (k / QB) & 1);
+      for (int c = max(0, ckv - NS); c < ckv; ++c) {
+        mbar_drain(bKfull(c % NS), (c / NS) & 1);
+        mbar_drain(bVfull(c % NS), (c / NS) & 1);
       }
-      if (ok && issue_pv(n_tiles - 1)) umma_commit(bOfinal);
+    } else if (warp == 1 && lane == 0) {
+      // ============================================================ MMA issuer
+      int nq[2] = {0, 0};    // items started per tile (Q buffer use)
+      int np[2] = {0, 0};    // P tiles consumed per tile
+      int nit[2] = {0, 0};   // items whose O was produced per tile
+      int ckv = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const Item it = decode_item(p, item);
+        const int c0 = ckv;
+        auto issue_qk = [&](int t, int j) -> bool {
+          const int c = c0 + (j - it.ubeg), s = c % NS;
+          if (!mbar_wait(bKfull(s), (c / NS) & 1, wc, kErrWaitKV)) return false;
+          tc_fence_after();
+          mma_qk<D, BF16>(tmem + t * 128, sdesc_sw128(sQ + (t * QB + (nq[t] % QB)) * C::kQBytes, 16, 1024),
+                          sdesc_sw128(sK + s * C::kTileBytes, 16, 1024));
+          umma_commit(bSfull(t));
+          if (j + 1 == it.end[t]) umma_commit(bQfree(t, nq[t] % QB));
+          return true;
+        };
+        auto issue_pv = [&](int t, int j) -> bool {
+          const int c = c0 + (j - it.ubeg), s = c % NS;
+          if (!mbar_wait(bPfull(t), np[t] & 1, wc, kErrWaitP)) return false;
+          np[t]++;
+          if (!mbar_wait(bVfull(s), (c / NS) & 1, wc, kErrWaitKV)) return false;
+          if (j == it.beg[t] && nit[t] > 0 && !mbar_wait(bOfree(t), (nit[t] - 1) & 1, wc, kErrWaitOFree))
+            return false;
+          tc_fence_after();
+          mma_pv<D, BF16>(tmem + C::kColO + t * D, tmem + t * 128,
+                          sdesc_sw128(sV + s * C::kTileBytes, C::kBoxBytes, 1024), (j > it.beg[t]) ? 1u : 0u);
+          if (j + 1 == it.end[t]) umma_commit(bOfinal(t));
+          return true;
+        };
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok && it.valid[t] && !mbar_wait(bQfull(t, nq[t] % QB), (nq[t] / QB) & 1, wc, kErrWaitQ)) ok = false;
+        for (int j = it.ubeg; ok && j < it.uend; ++j) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (ok && it.valid[t] && it.beg[t] == j) ok = issue_qk(t, j);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (ok && it.valid[t] && j >= it.beg[t] && j < it.end[t]) {
+              ok = issue_pv(t, j);
+              if (ok && j + 1 < it.end[t]) ok = issue_qk(t, j + 1);
+            }
+          }
+          if (ok) umma_commit(bKVempty((c0 + (j - it.ubeg)) % NS));
+        }
+        ckv = c0 + (it.uend - it.ubeg);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (it.valid[t]) {
+            nq[t]++;
+            nit[t]++;
+          }
+      }
       // Drain every MMA we issued before TMEM can be released.
       umma_commit(bDrain);
       mbar_drain(bDrain, 0);
     }
     __syncwarp();
   } else {
-    // ================================================================ softmax + epilogue
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    regs_inc<kRegsSoftmax>();
+    // ============================================================== softmax of tile t
+    const int t = wg - 1;
+    const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int pos = i0 + row + off;  // absolute position of this query row
+    const uint32_t scol = tmem + lane_off + t * 128;
+    const uint32_t ocol = tmem + lane_off + C::kColO + t * D;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
-    float l = 0.f;        // running sum of exp2(s * sl2 - m) in fp32 (gives LSE)
-    float lq = 0.f;       // the same sum over the 16-bit rounded probabilities (normalises O)
+    int ns = 0, nitems = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int kt = kv_begin + j;
-      const uint32_t scol = tmem + lane_off + (j & 1) * 128;
-      if (!mbar_wait_warp(bSfull(j & 1), (j >> 1) & 1, wc, kErrWaitS)) {
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const Item it = decode_item(p, item);
+      if (!it.valid[t]) continue;
+      const int pos = it.row0[t] + row + (p.Nk - p.Nq);  // absolute position of this query row
+      const int p0 = it.row0[t] + (p.Nk - p.Nq);
+      const int p1 = min(it.row0[t] + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
+      float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
+      float l = 0.f;        // running sum of exp2(s * sl2 - m), fp32
+      for (int j = it.beg[t]; j < it.end[t]; ++j) {
+        if (!mbar_wait_warp(bSfull(t), ns & 1, wc, kErrWaitS)) {
+          ok = false;
+          break;
+        }
+        ns++;
+        tc_fence_after();
+        uint32_t sr[kBN];
+        tmem_ld128(scol, sr);
+        const int key0 = j * kBN;
+        const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
+                               (p.window > 0 && key0 <= p1 - p.window);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (!key_live(key0 + c, pos, p.Nk, p.causal, p.window)) sr[c] = 0xff800000u;  // -inf
+        }
+        // row max: eight independent chains of 3-input max, then a short tree
+        float mx[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+        for (int c = 8; c < kBN; c += 16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+        }
+        const float mxa = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+        const float m_new = fmaxf(m, mxa * sl2);
+        // Lazy rescale: move the reference max only when it grew by more than
+        // 2^8 somewhere in the warp (the first tile of an item always sets it).
+        float alpha = 1.f;
+        const bool first = (j == it.beg[t]);
+        const bool rescale = !first && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
+        if (first || rescale) {
+          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+          m = m_new;
+        }
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        // p = 2^(s * sm_scale * log2 e - m), two elements per packed FMA
+        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
+        float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = ffma2(make_float2(__uint_as_float(sr[c * 32 + 2 * i]),
+                                               __uint_as_float(sr[c * 32 + 2 * i + 1])),
+                                   sl2x2, negm);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            pk[i] = pack2<BF16>(e.x, e.y);
+            rs[i & 1] = fadd2(rs[i & 1], e);
+          }
+          tmem_st16(scol + c * 16, pk);
+        }
+        l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
+        if (rescale) {
+          // S_t(j) is complete, so the P V of tile j-1 (issued before QK of
+          // tile j) is too: O_t can be rescaled before P V of tile j starts.
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(ocol + c * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(ocol + c * 32, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bPfull(t));
+      }
+      if (!ok) break;
+      // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2
+      if (!mbar_wait_warp(bOfinal(t), nitems & 1, wc, kErrWaitOFinal)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(scol + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-      }
-      const int key0 = kt * kBN;
-      const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
-                             (p.window > 0 && key0 <= p1 - p.window);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (!key_live(key0 + c, pos, p.Nk, p.causal, p.window)) s[c] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * sl2);
-      if (j == 0) {
-        m = m_new;
-      } else if (__any_sync(0xffffffffu, m_new > m + kRescaleLog2)) {
-        const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-        // O currently holds P_{j-1} V_{j-1}: wait for that MMA before touching it.
-        if (!mbar_wait_warp(bOdone, (j - 1) & 1, wc, kErrWaitO)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          const uint32_t ocol = tmem + lane_off + C::kColO + c * 32;
-          tmem_ld32(ocol, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(ocol, r);
-        }
-        l *= alpha;
-        lq *= alpha;
-        m = m_new;
-      }
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f, rsq = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float e0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
-          const float e1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
-          pk[i] = pack2<BF16>(e0, e1);
-          rs += e0 + e1;
-          // lq sums the 16-bit probabilities the P V contraction really uses,
-          // so the weights that normalise O add up to one.
-          const float2 r2 = unpack2<BF16>(pk[i]);
-          rsq += r2.x + r2.y;
-        }
-        tmem_st16(scol + c * 16, pk);
-      }
-      l += rs;
-      lq += rsq;
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bPfull(j & 1));
-    }
-    // ---- epilogue: O / l -> 16-bit, staged in the (now idle) Q buffer, TMA store; LSE.
-    if (ok) ok = mbar_wait_warp(bOfinal, 0, wc, kErrWaitOFinal);
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = (lq > 0.f) ? 1.f / lq : 0.f;
-      uint8_t *stage = smem + C::kOffQ;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const int grow = it.row0[t] + row;
+      const bool live_row = grow < p.Nq;
+      uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                      (static_cast<size_t>(it.bh[t]) * p.Nq + (live_row ? grow : 0)) * (D * 2);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::kColO + c * 32, r);
+        tmem_ld32(ocol + c * 32, r);
+        if (live_row) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col0 = c * 32 + q * 8;
-          const int box = col0 / 64, chunk = (col0 % 64) / 8;
-          uint4 w;
-          w.x = pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv_l, __uint_as_float(r[q * 8 + 1]) * inv_l);
-          w.y = pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv_l, __uint_as_float(r[q * 8 + 3]) * inv_l);
-          w.z = pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv_l, __uint_as_float(r[q * 8 + 5]) * inv_l);
-          w.w = pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv_l, __uint_as_float(r[q * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4 *>(stage + box * C::kBoxBytes + row * 128 + ((chunk ^ (row & 7)) * 16)) = w;
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv);
+            w.y = pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv);
+            w.z = pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
+            w.w = pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + c * 64 + q * 16) = w;
+          }
         }
       }
-      if (p.lse != nullptr && i0 + row < p.Nq) {
-        const float lse2 = (l > 0.f) ? m + log2f(l) : -INFINITY;
-        p.lse[static_cast<size_t>(bh) * p.Nq + i0 + row] = lse2 * 0.69314718055994530942f;
-      }
-      fence_proxy_async_smem();
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (warp == 2 && lane == 0 && ok && *abort_flag == 0) {
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_store_3d(&p.tmO, sQ + c * C::kBoxBytes, c * 64, i0, bh);
-      tma_store_commit();
-      tma_store_wait0();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bOfree(t));  // the next item's first P V may overwrite O_t
+      if (live_row && p.lse != nullptr)
+        p.lse[static_cast<size_t>(it.bh[t]) * p.Nq + grow] =
+            ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
+      nitems++;
     }
   }
   tc_fence_before();
