@@ -377,13 +377,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
       const Item it = decode_item(p, item);
-      if (!it.valid[t]) continue;
-      const int pos = it.row0[t] + row + (p.Nk - p.Nq);  // absolute position of this query row
-      const int p0 = it.row0[t] + (p.Nk - p.Nq);
-      const int p1 = min(it.row0[t] + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
+      // this warpgroup's tile, as scalars (t is not a compile-time index)
+      const bool tvalid = t ? it.valid[1] : it.valid[0];
+      if (!tvalid) continue;
+      const int trow0 = t ? it.row0[1] : it.row0[0];
+      const int tbeg = t ? it.beg[1] : it.beg[0];
+      const int tend = t ? it.end[1] : it.end[0];
+      const int tbh = t ? it.bh[1] : it.bh[0];
+      const int pos = trow0 + row + (p.Nk - p.Nq);  // absolute position of this query row
+      const int p0 = trow0 + (p.Nk - p.Nq);
+      const int p1 = min(trow0 + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
       float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
       float l = 0.f;        // running sum of exp2(s * sl2 - m), fp32
-      for (int j = it.beg[t]; j < it.end[t]; ++j) {
+      for (int j = tbeg; j < tend; ++j) {
         if (!mbar_wait_warp(bSfull(t), ns & 1, wc, kErrWaitS)) {
           ok = false;
           break;
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         // Lazy rescale: move the reference max only when it grew by more than
         // 2^8 somewhere in the warp (the first tile of an item always sets it).
         float alpha = 1.f;
-        const bool first = (j == it.beg[t]);
+        const bool first = (j == tbeg);
         const bool rescale = !first && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
         if (first || rescale) {
           alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
@@ -465,10 +471,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       }
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      const int grow = it.row0[t] + row;
+      const int grow = trow0 + row;
       const bool live_row = grow < p.Nq;
       uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                      (static_cast<size_t>(it.bh[t]) * p.Nq + (live_row ? grow : 0)) * (D * 2);
+                      (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       __syncwarp();
       if (lane == 0) mbar_arrive(bOfree(t));  // the next item's first P V may overwrite O_t
       if (live_row && p.lse != nullptr)
-        p.lse[static_cast<size_t>(it.bh[t]) * p.Nq + grow] =
+        p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
             ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
       nitems++;
     }
