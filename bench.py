@@ -189,6 +189,10 @@ def prepare(workload: str, device):
         c["flops"] = acc.shape_flops(shape)
         c["bytes"] = acc.shape_bytes(shape)
         c["label"] = call_label(shape)
+        # split-KV path (decode / few query rows): caller-provided workspace
+        wsb = attn.attn_fwd_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d)
+        c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device) if wsb > 0 else None
+        c["kernel"] = "attn_decode_kernel" if wsb > 0 else "attn_fwd_kernel"
         calls.append(c)
     return calls
 
@@ -197,9 +201,11 @@ def launch(c, stream_handle):
     import tiled_attention_forward_fwd_gb300 as attn
 
     s = c["shape"]
+    ws = c["ws"]
     st = attn.attn_fwd_ex(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["o"].data_ptr(),
                           c["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale,
-                          c["dtype_code"], None, 0, stream_handle)
+                          c["dtype_code"], None if ws is None else ws.data_ptr(),
+                          0 if ws is None else ws.numel(), stream_handle)
     if st != attn.ATTN_OK:
         raise RuntimeError(f"attn_fwd_ex failed: {attn.attn_status_string(st)}")
 
@@ -434,7 +440,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
     roof["traffic"] = profiled_traffic(args.workload, dc["label"])
-    roof["kernel"] = f"attn_fwd_kernel<{s.d},{'bf16' if s.dtype == 'bf16' else 'fp16'}> {dc['label']}"
+    roof["kernel"] = f"{dc['kernel']}<{s.d},{'bf16' if s.dtype == 'bf16' else 'fp16'}> {dc['label']}"
     roof["algorithmic"] = {"flops": dc["flops"], "bytes": dc["bytes"]}
     roof["peak_source"] = f"{peaks_src} (burst bf16 dense; fp16 same rate)" if roof["bound"] == "tensor" \
         else f"{peaks_src} HBM copy"

@@ -86,14 +86,17 @@ attn_status_t attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, 
                           int Hkv, int Nq, int Nk, int d, int causal, int window, float sm_scale,
                           attn_dtype_t dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Scratch bytes the split-KV path wants for this shape (0 when it would not
- * split). */
+/* Scratch bytes the split-KV path wants for this shape on the current device
+ * (0 when the shape does not take that path: it serves GQA groups of at most
+ * 32 query rows, i.e. (Hq / Hkv) * Nq <= 32, such as a decode step).  The
+ * size depends on the device's SM count, which sets the number of chunks. */
 size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.
- * dev_buf must hold attn_fwd_host_staging_bytes(...) bytes (256-byte aligned).
+ * dev_buf must hold attn_fwd_host_staging_bytes(...) bytes (256-byte aligned);
+ * that size includes the split-KV workspace when the shape takes that path.
  * The host buffers must stay valid until the stream reaches the end of the
  * call. */
 attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,

@@ -40,13 +40,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 3-D view (d, rows, slabs) of a dense (slabs, rows, d) 16-bit tensor, box
 // 64 x 128 x 1 with 128-byte swizzle.  Rows past `rows` read as zero and are
 // never written by stores.
-static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long slabs, bool bf16) {
+static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long slabs, bool bf16,
+                     int box_rows = 128) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(slabs)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * rows};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -154,21 +155,119 @@ static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *
               : launch_prefill<128, false>(Q, K, V, O, LSE, s, stream);
 }
 
+// ---------------------------------------------------------------- split-KV (decode) path
+struct DecPlan {
+  int nchunks = 0, chunk_keys = 0;
+  size_t bytes = 0;  // 0: this shape does not take the split-KV path
+};
+
+static int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// The split-KV path serves shapes whose GQA group holds at most 32 query rows
+// (decode: Nq = 1 with up to 32 query heads per K/V head).  Chunks are sized
+// so that about two CTAs per SM are in flight.
+static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  DecPlan pl;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return pl;
+  const long long R = static_cast<long long>(Hq / Hkv) * Nq;
+  if (R > kDecMaxRows) return pl;
+  const int sms = device_sm_count();
+  if (sms <= 0) return pl;
+  const long long units = static_cast<long long>(B) * Hkv;
+  if (units > 65535) return pl;  // grid.y limit
+  const int max_chunks = (Nk + kDecKeys - 1) / kDecKeys;
+  long long want = (2LL * sms + units - 1) / units;
+  int nchunks = static_cast<int>(std::max(1LL, std::min<long long>(want, max_chunks)));
+  int chunk_keys = (Nk + nchunks - 1) / nchunks;
+  chunk_keys = ((chunk_keys + kDecKeys - 1) / kDecKeys) * kDecKeys;
+  nchunks = (Nk + chunk_keys - 1) / chunk_keys;
+  pl.nchunks = nchunks;
+  pl.chunk_keys = chunk_keys;
+  pl.bytes = static_cast<size_t>(B) * Hq * Nq * nchunks * (d + 1) * sizeof(float);
+  return pl;
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  return decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes;
+}
+
+template <int D, bool BF16>
+static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                     const Shape &s, const DecPlan &pl, float *ws, int *status,
+                                     cudaStream_t stream) {
+  using Cfg = DecCfg<D>;
+  DecParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long zk = static_cast<long long>(s.B) * s.Hkv;
+  if (!make_map(&p.tmK, K, D, s.Nk, zk, BF16, kDecKeys) || !make_map(&p.tmV, V, D, s.Nk, zk, BF16, kDecKeys))
+    return ATTN_ERR_CUDA;
+  p.Q = Q;
+  p.ws = ws;
+  p.status = status;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Nq = s.Nq;
+  p.Nk = s.Nk;
+  p.group = s.Hq / s.Hkv;
+  p.R = p.group * s.Nq;
+  p.causal = s.causal ? 1 : 0;
+  p.window = s.window;
+  p.nchunks = pl.nchunks;
+  p.chunk_keys = pl.chunk_keys;
+  // keys some row of a group can see: all of them, except below the window
+  // of the first query row
+  p.kv_lo = (s.causal && s.window > 0) ? std::max(0, (s.Nk - s.Nq) - s.window + 1) : 0;
+  p.kv_hi = s.Nk;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  p.timeout_ns = g_timeout_ns.load();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  std::call_once(attr_once[dev], [&] {
+    cudaFuncSetAttribute(attn_decode_kernel<D, BF16, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::kSmemBytes);
+    cudaFuncSetAttribute(attn_decode_kernel<D, BF16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::kSmemBytes);
+  });
+  dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(zk));
+  if (p.R <= 16)
+    attn_decode_kernel<D, BF16, 1><<<grid, kDecThreads, Cfg::kSmemBytes, stream>>>(p);
+  else
+    attn_decode_kernel<D, BF16, 2><<<grid, kDecThreads, Cfg::kSmemBytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  const int rows = s.B * s.Hq * s.Nq;
+  attn_decode_combine_kernel<D, BF16><<<(rows + 3) / 4, 128, 0, stream>>>(ws, O, LSE, rows, pl.nchunks);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+static attn_status_t dispatch_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                     const Shape &s, const DecPlan &pl, float *ws, cudaStream_t stream) {
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
+  if (s.d == 64)
+    return bf16 ? launch_decode_t<64, true>(Q, K, V, O, LSE, s, pl, ws, status, stream)
+                : launch_decode_t<64, false>(Q, K, V, O, LSE, s, pl, ws, status, stream);
+  return bf16 ? launch_decode_t<128, true>(Q, K, V, O, LSE, s, pl, ws, status, stream)
+              : launch_decode_t<128, false>(Q, K, V, O, LSE, s, pl, ws, status, stream);
+}
+
 static attn_status_t run(const void *Q, const void *K, const void *V, void *O, float *LSE, const Shape &s,
                          void *ws, size_t ws_bytes, cudaStream_t stream) {
   attn_status_t st = validate(Q, K, V, O, LSE, s);
   if (st != ATTN_OK) return st;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
   if (ws != nullptr) {
-    const size_t need = decode_workspace_bytes(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d);
-    if (need > 0) {
-      if (ws_bytes < need || !aligned16(ws)) return ATTN_ERR_INVALID_ARG;
-      int *status = nullptr;
-      if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
-      return launch_decode(Q, K, V, O, LSE, s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.sm_scale,
-                           s.dtype == ATTN_DTYPE_BF16, ws, status, stream)
-                 ? ATTN_OK
-                 : ATTN_ERR_CUDA;
+    const DecPlan pl = decode_plan(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d);
+    if (pl.bytes > 0) {
+      if (ws_bytes < pl.bytes || !aligned16(ws)) return ATTN_ERR_INVALID_ARG;
+      return dispatch_decode(Q, K, V, O, LSE, s, pl, static_cast<float *>(ws), stream);
     }
   }
   return dispatch_prefill(Q, K, V, O, LSE, s, stream);
@@ -206,7 +305,8 @@ size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d
   const size_t q = static_cast<size_t>(B) * Hq * Nq * d * 2;
   const size_t kv = static_cast<size_t>(B) * Hkv * Nk * d * 2;
   const size_t lse = with_lse ? static_cast<size_t>(B) * Hq * Nq * 4 : 0;
-  return round_up256(q) * 2 + round_up256(kv) * 2 + round_up256(lse);
+  const size_t ws = decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+  return round_up256(q) * 2 + round_up256(kv) * 2 + round_up256(lse) + round_up256(ws);
 }
 
 attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
@@ -226,13 +326,16 @@ attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *
   void *dV = base + round_up256(q) + round_up256(kv);
   void *dO = base + round_up256(q) + 2 * round_up256(kv);
   float *dL = LSE_host ? reinterpret_cast<float *>(base + 2 * round_up256(q) + 2 * round_up256(kv)) : nullptr;
+  const size_t lse_bytes = LSE_host ? static_cast<size_t>(B) * Hq * Nq * 4 : 0;
+  const size_t ws_bytes = decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+  void *dW = ws_bytes ? base + 2 * round_up256(q) + 2 * round_up256(kv) + round_up256(lse_bytes) : nullptr;
   attn_status_t st = validate(dQ, dK, dV, dO, dL, s);
   if (st != ATTN_OK) return st;
   if (cudaMemcpyAsync(dQ, Q_host, q, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  st = run(dQ, dK, dV, dO, dL, s, nullptr, 0, stream);
+  st = run(dQ, dK, dV, dO, dL, s, dW, ws_bytes, stream);
   if (st != ATTN_OK) return st;
   if (cudaMemcpyAsync(O_host, dO, q, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   if (dL && cudaMemcpyAsync(LSE_host, dL, static_cast<size_t>(B) * Hq * Nq * 4, cudaMemcpyDeviceToHost, stream) !=

@@ -79,11 +79,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // is taken warp-wide, so the warp never diverges and stays converged for the
 // .sync.aligned tcgen05 instructions that follow.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl &w, int code) {
-#ifdef ATTN_WAIT_LANE0
-  int ok0 = 0;
-  if ((threadIdx.x & 31) == 0) ok0 = mbar_wait(bar, parity, w, code) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok0, 0) != 0;
-#endif
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
