@@ -61,7 +61,10 @@ typedef enum {
                                workspace too small */
   ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or no sm_100-family GPU */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-  ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded internal wait ran out */
+  ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded internal wait ran out */
+  ATTN_ERR_SCRATCH_LIMIT = 5 /* attn_fwd_decode_noalloc: the shape needs more than the
+                                library's built-in scratch, or does not take the
+                                split-KV path at all */
 } attn_status_t;
 
 typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
@@ -119,6 +122,33 @@ const char *attn_status_string(attn_status_t status);
 
 /* ATTN_ABI_VERSION of the loaded library. */
 int attn_abi_version(void);
+
+/* Split-KV decode that allocates nothing: the same computation as attn_fwd_ex
+ * with a workspace, but its scratch lives in a fixed array inside the
+ * library, so the caller passes only inputs and outputs.  The pages have no
+ * counterpart; it exists for callers that cannot hand the library any extra
+ * device memory, for example a host application whose device memory is all
+ * owned by its own pool and that offers plugins no allocation hook, or a
+ * serving loop that may not call cudaMalloc (which can synchronise the device)
+ * while requests are in flight.
+ *
+ * Q, K, V, O, LSE, sizes, masks, dtype and stream mean what they mean for
+ * attn_fwd_ex.  Only shapes that take the split-KV path qualify
+ * ((Hq / Hkv) * Nq <= 32), and their scratch (attn_fwd_workspace_bytes) must
+ * fit in the built-in 8 MiB; anything else returns ATTN_ERR_SCRATCH_LIMIT
+ * without launching.
+ *
+ * The scratch array is a single 8 MiB block per GPU, reserved for as long as
+ * the library is loaded.  Every call on a device uses the same block and
+ * leaves its contents behind; nothing in it needs to start at zero, because
+ * every value a call reads was written earlier in that call.  Calls whose
+ * work overlaps on the GPU (different streams without ordering between them)
+ * race on the block and give wrong results: order them on one stream.
+ * The first call on a device looks up the block's device address; make that
+ * first call before any stream capture begins on that device. */
+attn_status_t attn_fwd_decode_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                                      int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
+                                      float sm_scale, attn_dtype_t dtype, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -20,12 +20,14 @@ ATTN_ERR_INVALID_ARG = 1
 ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_SCRATCH_LIMIT = 5
 
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
-            "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version"]
+            "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
+            "attn_fwd_decode_noalloc"]
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_abi_version.argtypes = []
         L.attn_abi_version.restype = ci
+        L.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        L.attn_fwd_decode_noalloc.restype = ci
         del fp
         _lib = L
         return _lib
@@ -110,6 +114,14 @@ def attn_status_string(status: int) -> str:
 
 def attn_abi_version() -> int:
     return int(lib().attn_abi_version())
+
+
+def attn_fwd_decode_noalloc(Q, K, V, O, LSE, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype,
+                            stream) -> int:
+    """Split-KV decode whose scratch is a fixed block inside the library (for
+    callers that cannot provide device memory); see include/attn.h."""
+    return lib().attn_fwd_decode_noalloc(Q, K, V, O, LSE, B, Hq, Hkv, Nq, Nk, d, int(causal), int(window),
+                                         float(sm_scale), int(dtype), stream)
 
 
 # ------------------------------------------------------------------ torch-facing

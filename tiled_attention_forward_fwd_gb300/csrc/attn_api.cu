@@ -365,10 +365,52 @@ const char *attn_status_string(attn_status_t status) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension or device";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    case ATTN_ERR_SCRATCH_LIMIT: return "shape exceeds the built-in decode scratch";
   }
   return "unknown status";
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- decode without allocation
+// Scratch for attn_fwd_decode_noalloc: one fixed block per device, reserved
+// while the library is loaded.  In host code `g_decode_scratch` only names the
+// symbol; its device address comes from cudaGetSymbolAddress below.
+namespace attn {
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoallocScratchBytes];
+
+// Device address of the scratch block of the current device, looked up once
+// per device (with that device current).  nullptr if the lookup failed.
+static float *noalloc_scratch(int dev) {
+  static std::once_flag once[64];
+  static float *addr[64];
+  std::call_once(once[dev], [&] {
+    void *ptr = nullptr;
+    addr[dev] = (cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess) ? static_cast<float *>(ptr) : nullptr;
+  });
+  return addr[dev];
+}
+}  // namespace attn
+
+extern "C" {
+
+attn_status_t attn_fwd_decode_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                                      int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
+                                      float sm_scale, attn_dtype_t dtype, cudaStream_t stream) {
+  Shape s{B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype};
+  attn_status_t st = validate(Q, K, V, O, LSE, s);
+  if (st != ATTN_OK) return st;
+  int dev = -1;
+  if (current_device_sm_major(&dev) != 10) return ATTN_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, Nk, d);
+  if (pl.bytes == 0 || pl.bytes > kNoallocScratchBytes) return ATTN_ERR_SCRATCH_LIMIT;
+  float *scratch = noalloc_scratch(dev);
+  if (scratch == nullptr) return ATTN_ERR_CUDA;
+  return dispatch_decode(Q, K, V, O, LSE, s, pl, scratch, stream);
+}
 
 }  // extern "C"
