@@ -12,8 +12,10 @@
 // group size is even (each K/V tile load then serves both heads), else two
 // consecutive row tiles of one head.  12 warps in three warpgroups:
 //   WG0  warp 0: TMA producer -- Q tiles, then K_j / V_j into an NS-stage
-//                shared-memory ring (128B-swizzled boxes of 128 rows x 64 cols)
-//        warp 1: owns TMEM (512 columns) and issues tcgen05.mma from one lane:
+//                shared-memory ring (128B-swizzled boxes of 128 rows x 64 cols;
+//                K_j and V_j complete one barrier)
+//        warp 1: owns TMEM (512 columns) and issues tcgen05.mma from one
+//                elected lane of the converged warp:
 //                  S_t = Q_t K_j^T  (A, B in shared memory, fp32 in TMEM)
 //                  O_t += P_t V_j   (A = P_t in TMEM, B = V_j in shared memory)
 //                alternating between the two tiles so that one tile's
@@ -76,9 +78,9 @@ struct FwdCfg {
   static constexpr int kOffK = kOffQ + 2 * kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: qfull[2][QB], qfree[2][QB], kfull[NS], vfull[NS], kvempty[NS],
+  // barriers: qfull[2][QB], qfree[2][QB], kvfull[NS], kvempty[NS],
   //           sfull[2], pfull[2], ofinal[2], ofree[2], drain
-  static constexpr int kNumBars = 4 * kQBufs + 3 * kStages + 8 + 1;
+  static constexpr int kNumBars = 4 * kQBufs + 2 * kStages + 8 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
@@ -204,10 +206,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   const uint32_t bar0 = smem_u32(bars);
   auto bQfull = [&](int t, int q) { return bar0 + 8u * (t * QB + q); };
   auto bQfree = [&](int t, int q) { return bar0 + 8u * (2 * QB + t * QB + q); };
-  auto bKfull = [&](int s) { return bar0 + 8u * (4 * QB + s); };
-  auto bVfull = [&](int s) { return bar0 + 8u * (4 * QB + NS + s); };
-  auto bKVempty = [&](int s) { return bar0 + 8u * (4 * QB + 2 * NS + s); };
-  const uint32_t bX = bar0 + 8u * (4 * QB + 3 * NS);  // per-tile barriers follow
+  auto bKVfull = [&](int s) { return bar0 + 8u * (4 * QB + s); };
+  auto bKVempty = [&](int s) { return bar0 + 8u * (4 * QB + NS + s); };
+  const uint32_t bX = bar0 + 8u * (4 * QB + 2 * NS);  // per-tile barriers follow
   auto bSfull = [&](int t) { return bX + 8u * (0 + t); };
   auto bPfull = [&](int t) { return bX + 8u * (2 + t); };
   auto bOfinal = [&](int t) { return bX + 8u * (4 + t); };
@@ -231,8 +232,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       mbar_init(bOfree(t), 4);
     }
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bKfull(s), 1);
-      mbar_init(bVfull(s), 1);
+      mbar_init(bKVfull(s), 1);
       mbar_init(bKVempty(s), 1);
     }
     mbar_init(bDrain, 1);
@@ -250,11 +250,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
 
   if (wg == 0) {
     regs_dec<kRegsWG0>();
-    if (warp == 0 && lane == 0) {
+    // Both roles run their loops with the whole warp, so that control flow and
+    // addresses stay warp-uniform, and hand the issue of each TMA copy, MMA and
+    // commit to one elected lane.  A single-lane loop issues tcgen05.mma about
+    // twice as slowly, and at d = 64 that alone starves the tensor pipe.
+    if (warp == 0) {
       // ============================================================ TMA producer
-      tma_prefetch_desc(&p.tmQ);
-      tma_prefetch_desc(&p.tmK);
-      tma_prefetch_desc(&p.tmV);
+      if (elect_one()) {
+        tma_prefetch_desc(&p.tmQ);
+        tma_prefetch_desc(&p.tmK);
+        tma_prefetch_desc(&p.tmV);
+      }
+      __syncwarp();
       int nq[2] = {0, 0};
       int ckv = 0;
       bool ok = true;
@@ -264,79 +271,100 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         for (int t = 0; t < 2; ++t) {
           if (!ok || !it.valid[t]) continue;
           const int k = nq[t], q = k % QB;
-          if (k >= QB && !mbar_wait(bQfree(t, q), ((k / QB) - 1) & 1, wc, kErrWaitQFree)) {
+          if (k >= QB && !mbar_wait_warp(bQfree(t, q), ((k / QB) - 1) & 1, wc, kErrWaitQFree)) {
             ok = false;
             continue;
           }
           const uint32_t dst = sQ + (t * QB + q) * C::kQBytes;
-          mbar_arrive_expect_tx(bQfull(t, q), C::kQBytes);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bQfull(t, q), C::kQBytes);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(dst + c * C::kBoxBytes, &p.tmQ, bQfull(t, q), c * 64, it.row0[t], it.bh[t]);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(dst + c * C::kBoxBytes, &p.tmQ, bQfull(t, q), c * 64, it.row0[t], it.bh[t]);
+          }
+          __syncwarp();
           nq[t] = k + 1;
         }
         const int zkv = it.b * p.Hkv + it.kvh;
         for (int j = it.ubeg; ok && j < it.uend; ++j) {
           const int c = ckv, s = c % NS;
-          if (c >= NS && !mbar_wait(bKVempty(s), ((c / NS) - 1) & 1, wc, kErrWaitKVEmpty)) {
+          if (c >= NS && !mbar_wait_warp(bKVempty(s), ((c / NS) - 1) & 1, wc, kErrWaitKVEmpty)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bKfull(s), C::kTileBytes);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bKVfull(s), 2 * C::kTileBytes);
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc)
-            tma_load_3d(sK + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmK, bKfull(s), cc * 64, j * kBN, zkv);
-          mbar_arrive_expect_tx(bVfull(s), C::kTileBytes);
+            for (int cc = 0; cc < D / 64; ++cc)
+              tma_load_3d(sK + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmK, bKVfull(s), cc * 64, j * kBN, zkv);
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc)
-            tma_load_3d(sV + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmV, bVfull(s), cc * 64, j * kBN, zkv);
+            for (int cc = 0; cc < D / 64; ++cc)
+              tma_load_3d(sV + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmV, bKVfull(s), cc * 64, j * kBN, zkv);
+          }
+          __syncwarp();
           ckv = c + 1;
         }
       }
       // Never leave the CTA with one of our copies still in flight.
+      if (lane == 0) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
-        for (int k = max(0, nq[t] - QB); k < nq[t]; ++k) mbar_drain(bQfull(t, k % QB), (k / QB) & 1);
-      for (int c = max(0, ckv - NS); c < ckv; ++c) {
-        mbar_drain(bKfull(c % NS), (c / NS) & 1);
-        mbar_drain(bVfull(c % NS), (c / NS) & 1);
+        for (int t = 0; t < 2; ++t)
+          for (int k = max(0, nq[t] - QB); k < nq[t]; ++k) mbar_drain(bQfull(t, k % QB), (k / QB) & 1);
+        for (int c = max(0, ckv - NS); c < ckv; ++c) mbar_drain(bKVfull(c % NS), (c / NS) & 1);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ============================================================ MMA issuer
       int nq[2] = {0, 0};    // items started per tile (Q buffer use)
       int np[2] = {0, 0};    // P tiles consumed per tile
       int nit[2] = {0, 0};   // items whose O was produced per tile
-      int ckv = 0;
+      int ckv = 0;           // K/V ring slots consumed
+      int kv_seen = -1;      // last ring slot whose K/V arrival was waited for
       bool ok = true;
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
         const Item it = decode_item(p, item);
         const int c0 = ckv;
+        // S_t = Q_t K_j^T.  Both tiles read K_j, so the arrival of K_j / V_j is
+        // waited for once, by whichever tile gets there first.
         auto issue_qk = [&](int t, int j) -> bool {
           const int c = c0 + (j - it.ubeg), s = c % NS;
-          if (!mbar_wait(bKfull(s), (c / NS) & 1, wc, kErrWaitKV)) return false;
+          if (c > kv_seen) {
+            if (!mbar_wait_warp(bKVfull(s), (c / NS) & 1, wc, kErrWaitKV)) return false;
+            kv_seen = c;
+          }
           tc_fence_after();
-          mma_qk<D, BF16>(tmem + t * 128, sdesc_sw128(sQ + (t * QB + (nq[t] % QB)) * C::kQBytes, 16, 1024),
-                          sdesc_sw128(sK + s * C::kTileBytes, 16, 1024));
-          umma_commit(bSfull(t));
-          if (j + 1 == it.end[t]) umma_commit(bQfree(t, nq[t] % QB));
+          const uint64_t qd = sdesc_sw128(sQ + (t * QB + (nq[t] % QB)) * C::kQBytes, 16, 1024);
+          const uint64_t kd = sdesc_sw128(sK + s * C::kTileBytes, 16, 1024);
+          const bool last = (j + 1 == it.end[t]);
+          if (elect_one()) {
+            mma_qk<D, BF16>(tmem + t * 128, qd, kd);
+            umma_commit(bSfull(t));
+            if (last) umma_commit(bQfree(t, nq[t] % QB));
+          }
+          __syncwarp();
           return true;
         };
+        // O_t (+)= P_t V_j.  V_j arrived with K_j, before S_t(j) was issued.
         auto issue_pv = [&](int t, int j) -> bool {
-          const int c = c0 + (j - it.ubeg), s = c % NS;
-          if (!mbar_wait(bPfull(t), np[t] & 1, wc, kErrWaitP)) return false;
+          const int s = (c0 + (j - it.ubeg)) % NS;
+          if (!mbar_wait_warp(bPfull(t), np[t] & 1, wc, kErrWaitP)) return false;
           np[t]++;
-          if (!mbar_wait(bVfull(s), (c / NS) & 1, wc, kErrWaitKV)) return false;
-          if (j == it.beg[t] && nit[t] > 0 && !mbar_wait(bOfree(t), (nit[t] - 1) & 1, wc, kErrWaitOFree))
+          if (j == it.beg[t] && nit[t] > 0 && !mbar_wait_warp(bOfree(t), (nit[t] - 1) & 1, wc, kErrWaitOFree))
             return false;
           tc_fence_after();
-          mma_pv<D, BF16>(tmem + C::kColO + t * D, tmem + t * 128,
-                          sdesc_sw128(sV + s * C::kTileBytes, C::kBoxBytes, 1024), (j > it.beg[t]) ? 1u : 0u);
-          if (j + 1 == it.end[t]) umma_commit(bOfinal(t));
+          const uint64_t vd = sdesc_sw128(sV + s * C::kTileBytes, C::kBoxBytes, 1024);
+          const uint32_t acc = (j > it.beg[t]) ? 1u : 0u;
+          const bool last = (j + 1 == it.end[t]);
+          if (elect_one()) {
+            mma_pv<D, BF16>(tmem + C::kColO + t * D, tmem + t * 128, vd, acc);
+            if (last) umma_commit(bOfinal(t));
+          }
+          __syncwarp();
           return true;
         };
 #pragma unroll
         for (int t = 0; t < 2; ++t)
-          if (ok && it.valid[t] && !mbar_wait(bQfull(t, nq[t] % QB), (nq[t] / QB) & 1, wc, kErrWaitQ)) ok = false;
+          if (ok && it.valid[t] && !mbar_wait_warp(bQfull(t, nq[t] % QB), (nq[t] / QB) & 1, wc, kErrWaitQ))
+            ok = false;
         for (int j = it.ubeg; ok && j < it.uend; ++j) {
 #pragma unroll
           for (int t = 0; t < 2; ++t)
@@ -348,7 +376,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
               if (ok && j + 1 < it.end[t]) ok = issue_qk(t, j + 1);
             }
           }
-          if (ok) umma_commit(bKVempty((c0 + (j - it.ubeg)) % NS));
+          if (ok) {
+            if (elect_one()) umma_commit(bKVempty((c0 + (j - it.ubeg)) % NS));
+            __syncwarp();
+          }
         }
         ckv = c0 + (it.uend - it.ubeg);
 #pragma unroll
@@ -358,9 +389,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
             nit[t]++;
           }
       }
-      // Drain every MMA we issued before TMEM can be released.
-      umma_commit(bDrain);
-      mbar_drain(bDrain, 0);
+      // Drain every MMA we issued before TMEM can be released (the commit
+      // comes from the lane that issued them).
+      if (elect_one()) {
+        umma_commit(bDrain);
+        mbar_drain(bDrain, 0);
+      }
     }
     __syncwarp();
   } else {
