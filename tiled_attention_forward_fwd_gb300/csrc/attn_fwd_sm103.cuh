@@ -44,8 +44,6 @@ enum DeviceError : int {
   kErrWaitKV = 0x102,
   kErrWaitKVEmpty = 0x103,
   kErrWaitS = 0x104,
-  kErrWaitP = 0x105,
-  kErrWaitOFree = 0x106,
   kErrWaitOFinal = 0x107,
   kErrWaitQFree = 0x108,
 };
@@ -79,8 +77,8 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barriers: qfull[2][QB], qfree[2][QB], kvfull[NS], kvempty[NS],
-  //           sfull[2], pfull[2], ofinal[2], ofree[2], drain
-  static constexpr int kNumBars = 4 * kQBufs + 2 * kStages + 8 + 1;
+  //           sfull[2], ofinal[2], drain[2]
+  static constexpr int kNumBars = 4 * kQBufs + 2 * kStages + 6;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
@@ -210,10 +208,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   auto bKVempty = [&](int s) { return bar0 + 8u * (4 * QB + NS + s); };
   const uint32_t bX = bar0 + 8u * (4 * QB + 2 * NS);  // per-tile barriers follow
   auto bSfull = [&](int t) { return bX + 8u * (0 + t); };
-  auto bPfull = [&](int t) { return bX + 8u * (2 + t); };
-  auto bOfinal = [&](int t) { return bX + 8u * (4 + t); };
-  auto bOfree = [&](int t) { return bX + 8u * (6 + t); };
-  const uint32_t bDrain = bX + 8u * 8;
+  auto bOfinal = [&](int t) { return bX + 8u * (2 + t); };
+  auto bDrain = [&](int t) { return bX + 8u * (4 + t); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -227,15 +223,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         mbar_init(bQfree(t, q), 1);
       }
       mbar_init(bSfull(t), 1);
-      mbar_init(bPfull(t), 4);
       mbar_init(bOfinal(t), 1);
-      mbar_init(bOfree(t), 4);
+      mbar_init(bDrain(t), 1);
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bKVfull(s), 1);
-      mbar_init(bKVempty(s), 1);
+      mbar_init(bKVempty(s), 2);  // one arrival per query tile, whether or not it used the slot
     }
-    mbar_init(bDrain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -250,12 +244,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
 
   if (wg == 0) {
     regs_dec<kRegsWG0>();
-    // Both roles run their loops with the whole warp, so that control flow and
-    // addresses stay warp-uniform, and hand the issue of each TMA copy, MMA and
-    // commit to one elected lane.  A single-lane loop issues tcgen05.mma about
-    // twice as slowly, and at d = 64 that alone starves the tensor pipe.
     if (warp == 0) {
       // ============================================================ TMA producer
+      // The loop runs on the whole warp (uniform control flow and addresses);
+      // one elected lane issues each copy.
       if (elect_one()) {
         tma_prefetch_desc(&p.tmQ);
         tma_prefetch_desc(&p.tmK);
@@ -312,197 +304,192 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           for (int k = max(0, nq[t] - QB); k < nq[t]; ++k) mbar_drain(bQfull(t, k % QB), (k / QB) & 1);
         for (int c = max(0, ckv - NS); c < ckv; ++c) mbar_drain(bKVfull(c % NS), (c / NS) & 1);
       }
-    } else if (warp == 1) {
-      // ============================================================ MMA issuer
-      int nq[2] = {0, 0};    // items started per tile (Q buffer use)
-      int np[2] = {0, 0};    // P tiles consumed per tile
-      int nit[2] = {0, 0};   // items whose O was produced per tile
-      int ckv = 0;           // K/V ring slots consumed
-      int kv_seen = -1;      // last ring slot whose K/V arrival was waited for
-      bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-        const Item it = decode_item(p, item);
-        const int c0 = ckv;
-        // S_t = Q_t K_j^T.  Both tiles read K_j, so the arrival of K_j / V_j is
-        // waited for once, by whichever tile gets there first.
-        auto issue_qk = [&](int t, int j) -> bool {
-          const int c = c0 + (j - it.ubeg), s = c % NS;
-          if (c > kv_seen) {
-            if (!mbar_wait_warp(bKVfull(s), (c / NS) & 1, wc, kErrWaitKV)) return false;
-            kv_seen = c;
-          }
-          tc_fence_after();
-          const uint64_t qd = sdesc_sw128(sQ + (t * QB + (nq[t] % QB)) * C::kQBytes, 16, 1024);
-          const uint64_t kd = sdesc_sw128(sK + s * C::kTileBytes, 16, 1024);
-          const bool last = (j + 1 == it.end[t]);
-          if (elect_one()) {
-            mma_qk<D, BF16>(tmem + t * 128, qd, kd);
-            umma_commit(bSfull(t));
-            if (last) umma_commit(bQfree(t, nq[t] % QB));
-          }
-          __syncwarp();
-          return true;
-        };
-        // O_t (+)= P_t V_j.  V_j arrived with K_j, before S_t(j) was issued.
-        auto issue_pv = [&](int t, int j) -> bool {
-          const int s = (c0 + (j - it.ubeg)) % NS;
-          if (!mbar_wait_warp(bPfull(t), np[t] & 1, wc, kErrWaitP)) return false;
-          np[t]++;
-          if (j == it.beg[t] && nit[t] > 0 && !mbar_wait_warp(bOfree(t), (nit[t] - 1) & 1, wc, kErrWaitOFree))
-            return false;
-          tc_fence_after();
-          const uint64_t vd = sdesc_sw128(sV + s * C::kTileBytes, C::kBoxBytes, 1024);
-          const uint32_t acc = (j > it.beg[t]) ? 1u : 0u;
-          const bool last = (j + 1 == it.end[t]);
-          if (elect_one()) {
-            mma_pv<D, BF16>(tmem + C::kColO + t * D, tmem + t * 128, vd, acc);
-            if (last) umma_commit(bOfinal(t));
-          }
-          __syncwarp();
-          return true;
-        };
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (ok && it.valid[t] && !mbar_wait_warp(bQfull(t, nq[t] % QB), (nq[t] / QB) & 1, wc, kErrWaitQ))
-            ok = false;
-        for (int j = it.ubeg; ok && j < it.uend; ++j) {
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
-            if (ok && it.valid[t] && it.beg[t] == j) ok = issue_qk(t, j);
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (ok && it.valid[t] && j >= it.beg[t] && j < it.end[t]) {
-              ok = issue_pv(t, j);
-              if (ok && j + 1 < it.end[t]) ok = issue_qk(t, j + 1);
-            }
-          }
-          if (ok) {
-            if (elect_one()) umma_commit(bKVempty((c0 + (j - it.ubeg)) % NS));
-            __syncwarp();
-          }
-        }
-        ckv = c0 + (it.uend - it.ubeg);
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (it.valid[t]) {
-            nq[t]++;
-            nit[t]++;
-          }
-      }
-      // Drain every MMA we issued before TMEM can be released (the commit
-      // comes from the lane that issued them).
-      if (elect_one()) {
-        umma_commit(bDrain);
-        mbar_drain(bDrain, 0);
-      }
     }
     __syncwarp();
   } else {
     regs_inc<kRegsSoftmax>();
-    // ============================================================== softmax of tile t
+    // ============================================== softmax and MMA issue of tile t
     const int t = wg - 1;
     const int quad = warp & 3;
+    const bool issuer = (quad == 0);  // this warp issues the tile's MMAs from one elected lane
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t scol = tmem + lane_off + t * 128;
     const uint32_t ocol = tmem + lane_off + C::kColO + t * D;
+    const uint32_t named_bar = 1 + t;  // the 4 warps of this warpgroup
     const float sl2 = p.scale_log2;
-    int ns = 0, nitems = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+    int ns = 0, nfin = 0, nq = 0;
+    int ckv = 0;       // ring slots passed (both tiles walk every slot of every item)
+    int kv_seen = -1;  // last ring slot whose K/V arrival this warp has waited for
+    // `ok` is this thread's view (the issuer warp also fails on its own
+    // waits); `wg_ok` is the warpgroup's, agreed at every named barrier, and
+    // only it decides whether to leave a loop.
+    bool ok = true, wg_ok = true;
+    // issuer warp only: wait until ring slot c holds K_j / V_j
+    auto wait_kv = [&](int c) -> bool {
+      if (c <= kv_seen) return true;
+      if (!mbar_wait_warp(bKVfull(c % NS), (c / NS) & 1, wc, kErrWaitKV)) return false;
+      kv_seen = c;
+      return true;
+    };
+    // issuer warp only: a slot this tile does not read is released as soon as
+    // it is filled (so that the arrival counts towards this fill, not the last)
+    auto pass_slot = [&](int c) -> bool {
+      if (!wait_kv(c)) return false;
+      if (elect_one()) umma_commit(bKVempty(c % NS));
+      __syncwarp();
+      return true;
+    };
+    for (int item = blockIdx.x; wg_ok && item < p.n_items; item += gridDim.x) {
       const Item it = decode_item(p, item);
       // this warpgroup's tile, as scalars (t is not a compile-time index)
       const bool tvalid = t ? it.valid[1] : it.valid[0];
-      if (!tvalid) continue;
       const int trow0 = t ? it.row0[1] : it.row0[0];
-      const int tbeg = t ? it.beg[1] : it.beg[0];
-      const int tend = t ? it.end[1] : it.end[0];
+      const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
+      const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
       const int tbh = t ? it.bh[1] : it.bh[0];
+      const int c0 = ckv - it.ubeg;  // ring slot of K/V tile j is c0 + j
+      const int qbuf = nq % QB;
+      const uint32_t sQt = sQ + (t * QB + qbuf) * C::kQBytes;  // this tile's Q buffer
+      if (issuer) {
+        for (int j = it.ubeg; ok && j < tbeg; ++j) ok = pass_slot(c0 + j);
+        if (ok && tvalid) {
+          // the first S = Q K^T of this tile
+          ok = mbar_wait_warp(bQfull(t, qbuf), (nq / QB) & 1, wc, kErrWaitQ) && wait_kv(c0 + tbeg);
+          if (ok) {
+            tc_fence_after();
+            const uint64_t qd = sdesc_sw128(sQt, 16, 1024);
+            const uint64_t kd = sdesc_sw128(sK + ((c0 + tbeg) % NS) * C::kTileBytes, 16, 1024);
+            if (elect_one()) {
+              mma_qk<D, BF16>(tmem + t * 128, qd, kd);
+              umma_commit(bSfull(t));
+              if (tbeg + 1 == tend) umma_commit(bQfree(t, qbuf));
+            }
+            __syncwarp();
+          }
+        }
+      }
+      ckv = c0 + it.uend;
+      wg_ok = named_bar_and(named_bar, 128, ok);
+      if (!wg_ok) break;
+      if (!tvalid) continue;
+      nq++;
       const int pos = trow0 + row + (p.Nk - p.Nq);  // absolute position of this query row
       const int p0 = trow0 + (p.Nk - p.Nq);
       const int p1 = min(trow0 + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
       float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
       float l = 0.f;        // running sum of exp2(s * sl2 - m), fp32
       for (int j = tbeg; j < tend; ++j) {
-        if (!mbar_wait_warp(bSfull(t), ns & 1, wc, kErrWaitS)) {
-          ok = false;
-          break;
-        }
-        ns++;
-        tc_fence_after();
-        uint32_t sr[kBN];
-        tmem_ld128(scol, sr);
-        const int key0 = j * kBN;
-        const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
-                               (p.window > 0 && key0 <= p1 - p.window);
-        if (need_mask) {
+        // A failed wait still goes through this iteration's barrier, so that
+        // the whole warpgroup leaves together.
+        ok = ok && mbar_wait_warp(bSfull(t), ns & 1, wc, kErrWaitS);
+        if (ok) {
+          ns++;
+          tc_fence_after();
+          uint32_t sr[kBN];
+          tmem_ld128(scol, sr);
+          const int key0 = j * kBN;
+          const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
+                                 (p.window > 0 && key0 <= p1 - p.window);
+          if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (!key_live(key0 + c, pos, p.Nk, p.causal, p.window)) sr[c] = 0xff800000u;  // -inf
-        }
-        // row max: eight independent chains of 3-input max, then a short tree
-        float mx[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) mx[c] = __uint_as_float(sr[c]);
-#pragma unroll
-        for (int c = 8; c < kBN; c += 16) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
-        }
-        const float mxa = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
-        const float m_new = fmaxf(m, mxa * sl2);
-        // Lazy rescale: move the reference max only when it grew by more than
-        // 2^8 somewhere in the warp (the first tile of an item always sets it).
-        float alpha = 1.f;
-        const bool first = (j == tbeg);
-        const bool rescale = !first && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
-        if (first || rescale) {
-          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-          m = m_new;
-        }
-        const float mref = (m == -INFINITY) ? 0.f : m;
-        // p = 2^(s * sm_scale * log2 e - m), two elements per packed FMA
-        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
-        float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = ffma2(make_float2(__uint_as_float(sr[c * 32 + 2 * i]),
-                                               __uint_as_float(sr[c * 32 + 2 * i + 1])),
-                                   sl2x2, negm);
-            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            pk[i] = pack2<BF16>(e.x, e.y);
-            rs[i & 1] = fadd2(rs[i & 1], e);
+            for (int c = 0; c < kBN; ++c)
+              if (!key_live(key0 + c, pos, p.Nk, p.causal, p.window)) sr[c] = 0xff800000u;  // -inf
           }
-          tmem_st16(scol + c * 16, pk);
+          // row max: eight independent chains of 3-input max, then a short tree
+          float mx[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+          for (int c = 8; c < kBN; c += 16) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+          }
+          const float mxa = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+          const float m_new = fmaxf(m, mxa * sl2);
+          // Lazy rescale: move the reference max only when it grew by more
+          // than 2^8 somewhere in the warp (the first tile of an item always
+          // sets it).
+          float alpha = 1.f;
+          const bool first = (j == tbeg);
+          const bool rescale = !first && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
+          if (first || rescale) {
+            alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+            m = m_new;
+          }
+          const float mref = (m == -INFINITY) ? 0.f : m;
+          // p = 2^(s * sm_scale * log2 e - m), two elements per packed FMA
+          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
+          float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = ffma2(make_float2(__uint_as_float(sr[c * 32 + 2 * i]),
+                                                 __uint_as_float(sr[c * 32 + 2 * i + 1])),
+                                     sl2x2, negm);
+              const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              pk[i] = pack2<BF16>(e.x, e.y);
+              rs[i & 1] = fadd2(rs[i & 1], e);
+            }
+            tmem_st16(scol + c * 16, pk);
+          }
+          l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
+          if (rescale) {
+            // S_t(j) is complete, so the P V of tile j-1 (issued before the
+            // QK of tile j, by the same thread, on the in-order tensor pipe)
+            // is too: O_t can be rescaled before the P V of tile j is issued.
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(ocol + c * 32, r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(ocol + c * 32, r);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
         }
-        l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
-        if (rescale) {
-          // S_t(j) is complete, so the P V of tile j-1 (issued before QK of
-          // tile j) is too: O_t can be rescaled before P V of tile j starts.
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(ocol + c * 32, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(ocol + c * 32, r);
+        wg_ok = named_bar_and(named_bar, 128, ok);  // P_t(j) (and O_t) written by all four warps
+        if (!wg_ok) break;
+        if (issuer) {
+          const int c = c0 + j;
+          const bool more = (j + 1 < tend);
+          // Wait for the next K/V before issuing anything: with none of our
+          // MMAs in flight the check is cheap.
+          if (more) ok = wait_kv(c + 1);
+          if (ok) {
+            tc_fence_after();
+            const uint64_t vd = sdesc_sw128(sV + (c % NS) * C::kTileBytes, C::kBoxBytes, 1024);
+            const uint64_t qd = sdesc_sw128(sQt, 16, 1024);
+            const uint64_t kd = sdesc_sw128(sK + ((c + 1) % NS) * C::kTileBytes, 16, 1024);
+            const uint32_t acc = (j > tbeg) ? 1u : 0u;
+            if (elect_one()) {
+              mma_pv<D, BF16>(tmem + C::kColO + t * D, tmem + t * 128, vd, acc);
+              umma_commit(bKVempty(c % NS));
+              if (more) {
+                mma_qk<D, BF16>(tmem + t * 128, qd, kd);
+                umma_commit(bSfull(t));
+                if (j + 2 == tend) umma_commit(bQfree(t, qbuf));
+              } else {
+                umma_commit(bOfinal(t));
+              }
+            }
+            __syncwarp();
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bPfull(t));
       }
-      if (!ok) break;
+      if (!wg_ok) break;
+      if (issuer)
+        for (int j = tend; ok && j < it.uend; ++j) ok = pass_slot(c0 + j);
       // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2
-      if (!mbar_wait_warp(bOfinal(t), nitems & 1, wc, kErrWaitOFinal)) {
-        ok = false;
-        break;
-      }
+      ok = ok && mbar_wait_warp(bOfinal(t), nfin & 1, wc, kErrWaitOFinal);
+      wg_ok = named_bar_and(named_bar, 128, ok);
+      if (!wg_ok) break;
+      nfin++;
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       const int grow = trow0 + row;
@@ -525,14 +512,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           }
         }
       }
+      // The next item's first P V (accumulate = 0) overwrites O_t; it is
+      // issued after a named barrier that every warp reaches only after this
+      // read has completed (tcgen05.ld waits for its data).
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bOfree(t));  // the next item's first P V may overwrite O_t
       if (live_row && p.lse != nullptr)
         p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
             ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
-      nitems++;
     }
+    // Never release TMEM with one of our MMAs in flight: the commit comes from
+    // the lane that issued them.
+    if (issuer && elect_one()) {
+      umma_commit(bDrain(t));
+      mbar_drain(bDrain(t), 0);
+    }
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
