@@ -7,8 +7,10 @@ of the dominant kernel, next to the fp64 CPU oracle timed on the host cores.
 A step is one pass over every call of the workload (default ``mha_b2h4``:
 B=2, H=4, d=64, fp16, N in {256, 1024, 4096} x causal in {true, false}) with
 inputs resident in HBM.  The step is captured once as a CUDA graph and
-replayed; L2 is flushed (a 256 MiB write) between timed steps, outside the
-timed events.  Prints one JSON line (rank 0).
+replayed; L2 is flushed between timed steps, outside the timed events: a
+256 MiB write, then a 256 MiB read of another buffer, so that the timed step
+starts with none of its inputs in L2 and with no dirty lines of the flush
+left to write back.  Prints one JSON line (rank 0).
 """
 from __future__ import annotations
 
@@ -238,16 +240,23 @@ def device_timing(calls, steps, warmup, device, stream):
     import tiled_attention_forward_fwd_gb300 as attn
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    flush_rd = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def flush_l2():
+        flush.fill_(1.0)  # evicts everything (larger than the 129 MB L2) ...
+        flush_rd.sum()    # ... and this read leaves only clean lines behind
+
     g, evs = build_graph(calls, stream)
     t_start, t_stop = make_event(), make_event()
     for _ in range(warmup):
-        flush.fill_(1.0)
+        with torch.cuda.stream(stream):
+            flush_l2()
         g.replay()
     torch.cuda.synchronize(device)
     step_ms, call_ms = [], [[] for _ in calls]
     for _ in range(steps):
         with torch.cuda.stream(stream):
-            flush.fill_(0.0)
+            flush_l2()
             t_start.record(stream)
             g.replay()
             t_stop.record(stream)
@@ -472,7 +481,7 @@ def main():
             "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
                        "calls_per_step": len(calls),
                        "flop_convention": "4*B*Hq*N^2*d, halved for square causal; exact live pairs otherwise",
-                       "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                       "l2": "flushed between timed steps outside the timed events: 256 MiB write, then 256 MiB read",
                        "launch": "one CUDA graph per step", "parallelism": f"replicas x{ws}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": steps * len(calls), "clocks": clocks,

@@ -168,27 +168,63 @@ static int device_sm_count() {
   return n;
 }
 
+// Resident CTAs per SM of the split kernel for (d, row blocks), from the
+// occupancy calculator (shared memory and registers decide it).
+template <int D, int RB>
+static int decode_ctas_per_sm_t() {
+  using Cfg = DecCfg<D, RB>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  static int cache[64];
+  static std::once_flag once[64];
+  std::call_once(once[dev], [&] {
+    for (auto k : {attn_decode_kernel<D, true, RB>, attn_decode_kernel<D, false, RB>})
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<D, true, RB>, kDecThreads,
+                                                      Cfg::kSmemBytes) != cudaSuccess)
+      n = 0;
+    cache[dev] = n;
+  });
+  return cache[dev];
+}
+
+static int decode_ctas_per_sm(int d, int rb) {
+  if (d == 64) return rb == 1 ? decode_ctas_per_sm_t<64, 1>() : decode_ctas_per_sm_t<64, 2>();
+  return rb == 1 ? decode_ctas_per_sm_t<128, 1>() : decode_ctas_per_sm_t<128, 2>();
+}
+
 // The split-KV path serves shapes whose GQA group holds at most 32 query rows
-// (decode: Nq = 1 with up to 32 query heads per K/V head).  Chunks are sized
-// so that about two CTAs per SM are in flight.
+// (decode: Nq = 1 with up to 32 query heads per K/V head).  The number of
+// chunks per group minimises (waves of CTAs) x (K/V tiles per CTA + a fixed
+// cost of about two tiles per CTA): usually one full wave of resident CTAs.
 static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   DecPlan pl;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return pl;
   const long long R = static_cast<long long>(Hq / Hkv) * Nq;
   if (R > kDecMaxRows) return pl;
   const int sms = device_sm_count();
-  if (sms <= 0) return pl;
+  const int per_sm = decode_ctas_per_sm(d, R <= 16 ? 1 : 2);
+  if (sms <= 0 || per_sm <= 0) return pl;
   const long long units = static_cast<long long>(B) * Hkv;
   if (units > 65535) return pl;  // grid.y limit
-  const int max_chunks = (Nk + kDecKeys - 1) / kDecKeys;
-  long long want = (2LL * sms + units - 1) / units;
-  int nchunks = static_cast<int>(std::max(1LL, std::min<long long>(want, max_chunks)));
-  int chunk_keys = (Nk + nchunks - 1) / nchunks;
+  const long long slots = static_cast<long long>(sms) * per_sm;
+  const long long tiles = (Nk + kDecKeys - 1) / kDecKeys;
+  const long long max_n = std::min<long long>(std::min<long long>(tiles, kDecMaxChunks), 4 * slots / units + 1);
+  long long best_n = 1, best_cost = -1;
+  for (long long n = 1; n <= max_n; ++n) {
+    const long long waves = (units * n + slots - 1) / slots;
+    const long long cost = waves * ((tiles + n - 1) / n + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_n = n;
+    }
+  }
+  int chunk_keys = static_cast<int>((Nk + best_n - 1) / best_n);
   chunk_keys = ((chunk_keys + kDecKeys - 1) / kDecKeys) * kDecKeys;
-  nchunks = (Nk + chunk_keys - 1) / chunk_keys;
-  pl.nchunks = nchunks;
+  pl.nchunks = (Nk + chunk_keys - 1) / chunk_keys;
   pl.chunk_keys = chunk_keys;
-  pl.bytes = static_cast<size_t>(B) * Hq * Nq * nchunks * (d + 1) * sizeof(float);
+  pl.bytes = static_cast<size_t>(B) * Hq * Nq * pl.nchunks * (d + 1) * sizeof(float);
   return pl;
 }
 
@@ -200,7 +236,6 @@ template <int D, bool BF16>
 static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                      const Shape &s, const DecPlan &pl, float *ws, int *status,
                                      cudaStream_t stream) {
-  using Cfg = DecCfg<D>;
   DecParams p;
   std::memset(&p, 0, sizeof(p));
   const long long zk = static_cast<long long>(s.B) * s.Hkv;
@@ -208,6 +243,7 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
     return ATTN_ERR_CUDA;
   p.Q = Q;
   p.ws = ws;
+  p.ws_lse = ws + static_cast<size_t>(s.B) * s.Hq * s.Nq * pl.nchunks * D;
   p.status = status;
   p.B = s.B;
   p.Hq = s.Hq;
@@ -226,23 +262,32 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   p.kv_hi = s.Nk;
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  static std::once_flag attr_once[64];
-  std::call_once(attr_once[dev], [&] {
-    cudaFuncSetAttribute(attn_decode_kernel<D, BF16, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Cfg::kSmemBytes);
-    cudaFuncSetAttribute(attn_decode_kernel<D, BF16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Cfg::kSmemBytes);
-  });
+  // (the plan already set the shared-memory attribute of both kernels)
+  if (decode_ctas_per_sm(D, p.R <= 16 ? 1 : 2) <= 0) return ATTN_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(zk));
   if (p.R <= 16)
-    attn_decode_kernel<D, BF16, 1><<<grid, kDecThreads, Cfg::kSmemBytes, stream>>>(p);
+    attn_decode_kernel<D, BF16, 1><<<grid, kDecThreads, DecCfg<D, 1>::kSmemBytes, stream>>>(p);
   else
-    attn_decode_kernel<D, BF16, 2><<<grid, kDecThreads, Cfg::kSmemBytes, stream>>>(p);
+    attn_decode_kernel<D, BF16, 2><<<grid, kDecThreads, DecCfg<D, 2>::kSmemBytes, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  // The merge kernel is a programmatic dependent: it may launch while the
+  // split kernel runs and waits (griddepcontrol.wait) for its results.
   const int rows = s.B * s.Hq * s.Nq;
-  attn_decode_combine_kernel<D, BF16><<<(rows + 3) / 4, 128, 0, stream>>>(ws, O, LSE, rows, pl.nchunks);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = static_cast<size_t>(((pl.nchunks + 3) & ~3) + 128 / (D / 4) * D) * sizeof(float);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float *ws_c = ws, *ws_lse_c = p.ws_lse;
+  if (cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel<D, BF16>, ws_c, ws_lse_c, O, LSE, rows, pl.nchunks) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

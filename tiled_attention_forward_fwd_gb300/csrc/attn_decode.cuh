@@ -7,17 +7,23 @@
 // the chunks by rescaling each one with exp(m_p - m) * l_p and normalising by
 // the total.
 //
-// GB300 mapping.  Kernel 1, grid (chunks, B*Hkv), 128 threads: one CTA takes
-// the g*Nq query rows of one GQA group (all query heads that read the same
-// K/V head, up to 32 rows; they share every K/V tile) and one chunk of keys.
-// K/V tiles of 64 keys stream by TMA into a 3-stage ring (128B-swizzled boxes
-// of 64 rows x 64 columns); each of the 4 warps takes 16 keys of every tile
-// and keeps its own running max, sum and O for all rows, computed with
-// warp-level tensor-core MMAs (m16n8k16, fp32 accumulation); fragments come
-// from ldmatrix (transposed for V).  At the end the 4 warps are merged in
-// shared memory and the chunk's normalised O and its log2-domain log-sum-exp
-// go to the caller's workspace.  Kernel 2 merges the chunks of every row and
-// writes O (16-bit) and LSE.
+// GB300 mapping.  Kernel 1, grid (chunks, B*Hkv), sized by the host to one
+// wave of resident CTAs: one CTA takes the g*Nq query rows of one GQA group
+// (all query heads that read the same K/V head, up to 32 rows; they share
+// every K/V tile) and one chunk of keys.  A producer warp streams K/V tiles of
+// 64 keys by TMA into a 3-stage ring (128B-swizzled boxes of 64 rows x 64
+// columns) while the query rows are staged; K and V of a stage have their own
+// full / empty barriers, so K of tile i+3 is requested as soon as every warp
+// has finished Q K^T of tile i.  Each of the 4 consumer warps takes 16 keys
+// of every tile and keeps its own running max, sum and O for all rows,
+// computed with warp-level tensor-core MMAs (m16n8k16, fp32 accumulation; the
+// work is bandwidth-bound, so the legacy MMA is enough); fragments come from
+// ldmatrix (transposed for V), and O is rescaled only when a row's max grew
+// by more than 2^8.  At the end the 4 warps are merged in shared memory and
+// the chunk's normalised O and its log2-domain log-sum-exp go to the
+// caller's workspace.  Kernel 2, launched as a programmatic dependent so that
+// its launch overlaps kernel 1, merges the chunks of every row (one CTA per
+// row) and writes O (16-bit) and LSE.
 #pragma once
 
 #include <stddef.h>
@@ -27,10 +33,10 @@
 namespace attn {
 
 constexpr int kDecKeys = 64;     // keys per K/V tile
-constexpr int kDecStages = 3;    // K/V ring depth
-constexpr int kDecWarps = 4;     // each warp owns 16 keys of every tile
-constexpr int kDecThreads = 32 * kDecWarps;
+constexpr int kDecWarps = 4;     // consumer warps: each owns 16 keys of every tile
+constexpr int kDecThreads = 32 * kDecWarps + 32;  // + one TMA producer warp
 constexpr int kDecMaxRows = 32;  // query rows of one group handled by one CTA
+constexpr int kDecMaxChunks = 1024;  // key chunks per group (bounds the merge kernel's shared memory)
 
 enum DecodeError : int { kErrDecWaitKV = 0x201 };
 
@@ -38,7 +44,8 @@ struct DecParams {
   CUtensorMap tmK;  // (d, Nk, B*Hkv), box 64 x 64 x 1, 128B swizzle
   CUtensorMap tmV;
   const void *Q;    // (B, Hq, Nq, d), 16-bit
-  float *ws;        // [B*Hq*Nq][nchunks][d + 1]: normalised O of the chunk, then its log2 LSE
+  float *ws;        // [B*Hq*Nq][nchunks][d]: normalised O of each chunk
+  float *ws_lse;    // [B*Hq*Nq][nchunks]: log2 LSE of each chunk (-inf: no live key)
   int *status;
   int B, Hq, Hkv, Nq, Nk, group, R;  // R = group * Nq query rows per CTA
   int causal, window;
@@ -48,18 +55,30 @@ struct DecParams {
   unsigned long long timeout_ns;
 };
 
-template <int D>
+// Ring depth and resident CTAs per SM for (d, row blocks).  Tiles arrive
+// about 3 us after they are requested when HBM is busy, so the ring holds as
+// many as shared memory allows: 3 stages x 2 CTAs at d = 128 with up to 16
+// rows; 6 stages x 1 CTA for 32 rows at d = 128 (whose per-thread O state
+// does not fit two CTAs' registers without spilling); 6 stages x 2 CTAs at
+// d = 64.
+template <int D, int RB>
 struct DecCfg {
+  static constexpr int kStages = (D == 128 && RB == 1) ? 3 : 6;
+  static constexpr int kMinCtas = (D == 128 && RB == 2) ? 1 : 2;
   static constexpr int kBoxBytes = kDecKeys * 128;          // 64 rows x 128 B
   static constexpr int kTileBytes = kDecKeys * D * 2;       // one K or V tile
   static constexpr int kQBoxBytes = kDecMaxRows * 128;      // 32 rows x 128 B
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = ((kDecMaxRows * D * 2 + 1023) / 1024) * 1024;
   static constexpr int kStageBytes = 2 * kTileBytes;        // K then V
-  static constexpr int kOffBar = kOffKV + kDecStages * kStageBytes;
-  static constexpr int kOffStats = kOffBar + 64;            // float wm[4][32], wl[4][32]
-  static constexpr int kSmemBytes = kOffStats + 2 * kDecWarps * kDecMaxRows * 4 + 1024;
-  static_assert(kDecWarps * kDecMaxRows * D * 4 <= kDecStages * kStageBytes, "O merge slabs fit in the ring");
+  static constexpr int kOffBar = kOffKV + kStages * kStageBytes;  // kfull, vfull, kempty, vempty [stages]; abort
+  static constexpr int kOffStats = kOffBar + 256;           // float wm[4][32], wl[4][32], rinv[32]
+  static constexpr int kSmemBytes = kOffStats + (2 * kDecWarps + 1) * kDecMaxRows * 4 + 1024;
+  static constexpr int kSlabStride = D + 8;                 // floats per merge-slab row (2-way bank conflicts)
+  static_assert(kDecWarps * kDecMaxRows * kSlabStride * 4 <= kStages * kStageBytes,
+                "O merge slabs fit in the ring");
+  static_assert(4 * kStages * 8 + 4 <= 256, "barriers fit");
+  static_assert(kMinCtas * (kSmemBytes + 1024) <= 233472, "shared memory per SM");
 };
 
 // Byte offset of element (row r, column c) in a stack of 64-column boxes of
@@ -96,19 +115,34 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
   }
 }
 
+// Bounded wait that ignores the abort flag: used only to drain our own
+// copies, which always complete.
+__device__ __forceinline__ void mbar_drain_dec(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 1000000000ull) break;
+}
+
 // Partial attention of one GQA group over one key chunk.  RB = row blocks of
 // 16 (1: up to 16 rows, 2: up to 32).
 template <int D, bool BF16, int RB>
-__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_constant__ DecParams p) {
-  using C = DecCfg<D>;
+__global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
+    attn_decode_kernel(const __grid_constant__ DecParams p) {
+  using C = DecCfg<D, RB>;
+  constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-  int *abort_flag = reinterpret_cast<int *>(full + kDecStages);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  int *abort_flag = reinterpret_cast<int *>(bars + 4 * NS);
   float *wm = reinterpret_cast<float *>(smem + C::kOffStats);  // [warp][row] running max (log2 domain)
   float *wl = wm + kDecWarps * kDecMaxRows;                    // [warp][row] running sum
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sKV = smem_u32(smem + C::kOffKV);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bKfull = [&](int s) { return bar0 + 8u * s; };
+  auto bVfull = [&](int s) { return bar0 + 8u * (NS + s); };
+  auto bKempty = [&](int s) { return bar0 + 8u * (2 * NS + s); };
+  auto bVempty = [&](int s) { return bar0 + 8u * (3 * NS + s); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
@@ -120,40 +154,79 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
   const int ntiles = (k1 > k0) ? (k1 - k0 + kDecKeys - 1) / kDecKeys : 0;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
+  // Let the merge kernel launch now; it waits for this grid to finish
+  // before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < kDecStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bKfull(s), 1);
+      mbar_init(bVfull(s), 1);
+      mbar_init(bKempty(s), kDecWarps);
+      mbar_init(bVempty(s), kDecWarps);
+    }
     fence_mbar_init();
   }
-  // the group's query rows -> shared memory (swizzled like a 32-row box); rows >= R are zero
-  for (int idx = threadIdx.x; idx < kDecMaxRows * (D / 8); idx += kDecThreads) {
-    const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < p.R) {
-      const int head = kvh * p.group + r / p.Nq, i = r % p.Nq;
-      v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.Q) +
-                                           ((static_cast<size_t>(b) * p.Hq + head) * p.Nq + i) * D + c8);
-    }
-    *reinterpret_cast<uint4 *>(smem + C::kOffQ + swz(kDecMaxRows, r, c8)) = v;
-  }
   __syncthreads();
+  bool ok = true;
 
-  auto issue = [&](int tile) {
-    const int s = tile % kDecStages;
-    const uint32_t bar = smem_u32(&full[s]);
-    const uint32_t kdst = sKV + s * C::kStageBytes, vdst = kdst + C::kTileBytes;
-    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-#pragma unroll
-    for (int cc = 0; cc < D / 64; ++cc) {
-      tma_load_3d(kdst + cc * C::kBoxBytes, &p.tmK, bar, cc * 64, k0 + tile * kDecKeys, bk);
-      tma_load_3d(vdst + cc * C::kBoxBytes, &p.tmV, bar, cc * 64, k0 + tile * kDecKeys, bk);
+  if (warp == kDecWarps) {
+    // ======================================================== TMA producer
+    // K of tile i goes out as soon as every consumer warp has finished Q K^T
+    // of tile i - NS, V as soon as they have finished P V of it.
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tmK);
+      tma_prefetch_desc(&p.tmV);
     }
-  };
-  int issued = 0;
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&p.tmK);
-    tma_prefetch_desc(&p.tmV);
-    for (; issued < min(kDecStages, ntiles); ++issued) issue(issued);
+    __syncwarp();
+    int kiss = 0, viss = 0;  // K / V tiles issued
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % NS, y = k0 + i * kDecKeys;
+      const uint32_t kdst = sKV + s * C::kStageBytes, vdst = kdst + C::kTileBytes;
+      if (i >= NS && !mbar_wait_warp(bKempty(s), ((i / NS) - 1) & 1, wc, kErrDecWaitKV)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bKfull(s), C::kTileBytes);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(kdst + cc * C::kBoxBytes, &p.tmK, bKfull(s), cc * 64, y, bk);
+      }
+      __syncwarp();
+      kiss = i + 1;
+      if (i >= NS && !mbar_wait_warp(bVempty(s), ((i / NS) - 1) & 1, wc, kErrDecWaitKV)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bVfull(s), C::kTileBytes);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(vdst + cc * C::kBoxBytes, &p.tmV, bVfull(s), cc * 64, y, bk);
+      }
+      __syncwarp();
+      viss = i + 1;
+    }
+    if (!ok && lane == 0) {
+      // Never leave with one of our copies in flight: wait (bounded) for the
+      // last loads issued into each stage.
+      for (int i = max(0, kiss - NS); i < kiss; ++i) mbar_drain_dec(bKfull(i % NS), (i / NS) & 1);
+      for (int i = max(0, viss - NS); i < viss; ++i) mbar_drain_dec(bVfull(i % NS), (i / NS) & 1);
+    }
+  } else {
+    // ======================================================== consumer warps
+    // the group's query rows -> shared memory (swizzled like a 32-row box); rows >= R are zero
+    for (int idx = threadIdx.x; idx < kDecMaxRows * (D / 8); idx += 32 * kDecWarps) {
+      const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < p.R) {
+        const int head = kvh * p.group + r / p.Nq, i = r % p.Nq;
+        v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.Q) +
+                                             ((static_cast<size_t>(b) * p.Hq + head) * p.Nq + i) * D + c8);
+      }
+      *reinterpret_cast<uint4 *>(smem + C::kOffQ + swz(kDecMaxRows, r, c8)) = v;
+    }
+    named_bar_and(1, 32 * kDecWarps, true);  // Q staged (consumer warps only)
   }
 
   // running state: rows rb*16 + g (h = 0) and rb*16 + g + 8 (h = 1)
@@ -175,13 +248,11 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
     for (int n = 0; n < D / 8; ++n) o[rb][n][0] = o[rb][n][1] = o[rb][n][2] = o[rb][n][3] = 0.f;
   }
   const float sl2 = p.scale_log2;
-  bool aborted = false;
 
-  for (int i = 0; i < ntiles; ++i) {
-    const int s = i % kDecStages;
-    const bool ok = mbar_wait_warp(smem_u32(&full[s]), (i / kDecStages) & 1, wc, kErrDecWaitKV);
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
+  for (int i = 0; warp < kDecWarps && i < ntiles; ++i) {
+    const int s = i % NS;
+    if (!mbar_wait_warp(bKfull(s), (i / NS) & 1, wc, kErrDecWaitKV)) {
+      ok = false;
       break;
     }
     const uint32_t sK = sKV + s * C::kStageBytes, sV = sK + C::kTileBytes;
@@ -209,6 +280,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bKempty(s));  // this warp is done with K of tile i
     // ---- mask, online softmax (log2 domain), P as A fragments
     uint32_t pa[RB][4];
 #pragma unroll
@@ -229,25 +302,34 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         float tmax = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+        // Lazy rescale: the reference max moves only when it grew by more
+        // than 2^8 for some row of this warp, so O is rarely rescaled.
         const float m_new = fmaxf(m[rb][h], tmax * sl2);
-        const float alpha = (m[rb][h] == -INFINITY) ? 0.f : ex2_approx(m[rb][h] - m_new);
-        const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+        if (__any_sync(0xffffffffu, m_new > m[rb][h] + 8.0f)) {
+          const float alpha = (m[rb][h] == -INFINITY) ? 0.f : ex2_approx(m[rb][h] - m_new);
+          l[rb][h] *= alpha;
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            o[rb][n][2 * h] *= alpha;
+            o[rb][n][2 * h + 1] *= alpha;
+          }
+          m[rb][h] = m_new;
+        }
+        const float mref = (m[rb][h] == -INFINITY) ? 0.f : m[rb][h];
         float e4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) e4[q] = ex2_approx(fmaf(v[q], sl2, -mref));
-        l[rb][h] = l[rb][h] * alpha + ((e4[0] + e4[1]) + (e4[2] + e4[3]));
-        m[rb][h] = m_new;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          o[rb][n][2 * h] *= alpha;
-          o[rb][n][2 * h + 1] *= alpha;
-        }
+        l[rb][h] += (e4[0] + e4[1]) + (e4[2] + e4[3]);
         // A fragment of P: a0/a2 hold row g (keys 2t, 8+2t), a1/a3 row g+8
         pa[rb][h] = pack2<BF16>(e4[0], e4[1]);
         pa[rb][2 + h] = pack2<BF16>(e4[2], e4[3]);
       }
     }
     // ---- O += P V
+    if (!mbar_wait_warp(bVfull(s), (i / NS) & 1, wc, kErrDecWaitKV)) {
+      ok = false;
+      break;
+    }
     {
       const int j = lane >> 3;
       const int vrow = warp * 16 + (j & 1) * 8 + (lane & 7);
@@ -262,58 +344,50 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         }
       }
     }
-    __syncthreads();  // every warp is done with stage s
-    if (threadIdx.x == 0 && issued < ntiles) issue(issued++);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bVempty(s));  // this warp is done with V of tile i
   }
-  if (aborted) {
-    // Never leave with one of our copies in flight: wait (bounded) for the
-    // last loads issued into each stage.
-    if (threadIdx.x == 0) {
-      for (int t = max(0, issued - kDecStages); t < issued; ++t) {
-        const uint32_t bar = smem_u32(&full[t % kDecStages]);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar, (t / kDecStages) & 1))
-          if (globaltimer_ns() - t0 > 1000000000ull) break;
-      }
-    }
-    return;
-  }
+  // Every thread learns whether any role gave up; then nothing is in flight
+  // (the producer drained its copies above) and the CTA can leave.
+  if (__syncthreads_or(!ok)) return;
 
   // ---- merge the 4 warps: row sums over the quad, then max / sums per row in shared memory
+  const bool consumer = warp < kDecWarps;
 #pragma unroll
   for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       l[rb][h] += __shfl_xor_sync(0xffffffffu, l[rb][h], 1);
       l[rb][h] += __shfl_xor_sync(0xffffffffu, l[rb][h], 2);
-      if (tq == 0) {
+      if (consumer && tq == 0) {
         const int r = rb * 16 + g + 8 * h;
         wm[warp * kDecMaxRows + r] = m[rb][h];
         wl[warp * kDecMaxRows + r] = l[rb][h];
       }
     }
   // one slab per warp, summed in a fixed order below (deterministic result)
-  float *oacc = reinterpret_cast<float *>(smem + C::kOffKV);  // [warp][32][D], the ring is idle now
+  float *oacc = reinterpret_cast<float *>(smem + C::kOffKV);  // [warp][32][kSlabStride], the ring is idle now
+  float *rinv = wl + kDecWarps * kDecMaxRows;                  // [row] 1 / (chunk sum)
   __syncthreads();
 #pragma unroll
   for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+      if (!consumer) continue;
       const int r = rb * 16 + g + 8 * h;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * kDecMaxRows + r]);
       const float scale = (m[rb][h] == -INFINITY) ? 0.f : ex2_approx(m[rb][h] - M);
-      float *slab = oacc + (warp * kDecMaxRows + r) * D;
+      float *slab = oacc + (warp * kDecMaxRows + r) * C::kSlabStride;
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
         *reinterpret_cast<float2 *>(slab + n * 8 + 2 * tq) =
             make_float2(o[rb][n][2 * h] * scale, o[rb][n][2 * h + 1] * scale);
     }
-  __syncthreads();
-  // ---- this chunk's normalised O and log2 LSE per row -> workspace
-  for (int idx = threadIdx.x; idx < p.R * (D + 1); idx += kDecThreads) {
-    const int r = idx / (D + 1), c = idx - r * (D + 1);
+  // per-row totals, once per row: the chunk's log2 LSE and 1 / sum
+  if (threadIdx.x < p.R) {
+    const int r = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * kDecMaxRows + r]);
@@ -323,52 +397,98 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
       const float mw = wm[w * kDecMaxRows + r];
       if (mw != -INFINITY) L += ex2_approx(mw - M) * wl[w * kDecMaxRows + r];
     }
+    rinv[r] = (L > 0.f) ? 1.f / L : 0.f;
     const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
     const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
-    float *dst = p.ws + (grow * p.nchunks + chunk) * (D + 1);
-    if (c < D) {
-      float acc = 0.f;
+    p.ws_lse[grow * p.nchunks + chunk] = (L > 0.f) ? M + log2f(L) : -INFINITY;
+  }
+  __syncthreads();
+  // ---- this chunk's normalised O -> workspace, four columns per thread
+  for (int idx = threadIdx.x; idx < p.R * (D / 4); idx += kDecThreads) {
+    const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+    float4 acc = *reinterpret_cast<const float4 *>(oacc + r * C::kSlabStride + c);
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) acc += oacc[(w * kDecMaxRows + r) * D + c];
-      dst[c] = (L > 0.f) ? acc / L : 0.f;
+    for (int w = 1; w < kDecWarps; ++w) {
+      const float4 v = *reinterpret_cast<const float4 *>(oacc + (w * kDecMaxRows + r) * C::kSlabStride + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
     }
-    else dst[D] = (L > 0.f) ? M + log2f(L) : -INFINITY;
+    const float inv = rinv[r];
+    const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
+    const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
+    *reinterpret_cast<float4 *>(p.ws + (grow * p.nchunks + chunk) * D + c) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
 }
 
 // Merge the chunks of every query row: O = sum_c 2^(lse_c - lse) o_c,
-// LSE = lse * ln 2 with lse = log2 sum_c 2^(lse_c).  One warp per row.
+// LSE = lse * ln 2 with lse = log2 sum_c 2^(lse_c).  One CTA of 128 threads
+// per row: the chunk weights go to shared memory, then D/4 threads per chunk
+// row read four columns each (float4) and the 128 / (D/4) groups of chunks
+// are summed in a fixed order.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const float *ws, void *O, float *lse, int rows,
-                                                                  int nchunks) {
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const float *ws, const float *ws_lse, void *O,
+                                                                  float *lse, int rows, int nchunks) {
+  extern __shared__ float wts[];  // [nchunks] weights, then [groups][D] partial sums
+  __shared__ float red[4];
+  // Launched as a programmatic dependent of the split kernel: wait until it
+  // has finished and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int row = blockIdx.x;
   if (row >= rows) return;
-  const float *base = ws + static_cast<size_t>(row) * nchunks * (D + 1);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float *lrow = ws_lse + static_cast<size_t>(row) * nchunks;
   float M = -INFINITY;
-  for (int c = lane; c < nchunks; c += 32) M = fmaxf(M, base[c * (D + 1) + D]);
+  for (int c = tid; c < nchunks; c += 128) M = fmaxf(M, lrow[c]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[D / 32];
-#pragma unroll
-  for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
-  float L = 0.f;
-  for (int c = 0; c < nchunks; ++c) {
-    const float lc = base[c * (D + 1) + D];
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float Ls = 0.f;
+  for (int c = tid; c < nchunks; c += 128) {
+    const float lc = lrow[c];
     const float w = (lc == -INFINITY) ? 0.f : ex2_approx(lc - M);
-    L += w;
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) acc[k] += w * base[c * (D + 1) + lane + 32 * k];
+    wts[c] = w;
+    Ls += w;
   }
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  uint16_t *orow = reinterpret_cast<uint16_t *>(O) + static_cast<size_t>(row) * D;
 #pragma unroll
-  for (int k = 0; k < D / 32; ++k) {
-    const uint32_t pk = pack2<BF16>(acc[k] * inv, 0.f);
-    orow[lane + 32 * k] = static_cast<uint16_t>(pk & 0xFFFFu);
+  for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+  if (lane == 0) red[warp] = Ls;
+  __syncthreads();
+  const float L = (red[0] + red[1]) + (red[2] + red[3]);
+  constexpr int kTpr = D / 4;          // threads per chunk row
+  constexpr int kGroups = 128 / kTpr;  // chunk groups
+  const int grp = tid / kTpr, col = (tid % kTpr) * 4;
+  const float *orow = ws + static_cast<size_t>(row) * nchunks * D + col;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int c = grp; c < nchunks; c += kGroups) {
+    const float w = wts[c];
+    const float4 v = *reinterpret_cast<const float4 *>(orow + static_cast<size_t>(c) * D);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
-  if (lse != nullptr && lane == 0)
-    lse[row] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+  float *part = wts + ((nchunks + 3) & ~3);  // 16-byte aligned
+  *reinterpret_cast<float4 *>(part + grp * D + col) = acc;
+  __syncthreads();
+  if (tid < D / 2) {
+    const int c2 = tid * 2;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      a0 += part[g * D + c2];
+      a1 += part[g * D + c2 + 1];
+    }
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    reinterpret_cast<uint32_t *>(O)[(static_cast<size_t>(row) * D + c2) / 2] = pack2<BF16>(a0 * inv, a1 * inv);
+  }
+  if (lse != nullptr && tid == 0) lse[row] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace attn
