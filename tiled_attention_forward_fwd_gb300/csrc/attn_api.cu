@@ -14,6 +14,7 @@
 
 #include "../../include/attn.h"
 #include "attn_decode.cuh"
+#include "attn_short.cuh"
 #include "attn_fwd_sm103.cuh"
 
 namespace attn {
@@ -303,11 +304,90 @@ static attn_status_t dispatch_decode(const void *Q, const void *K, const void *V
               : launch_decode_t<128, false>(Q, K, V, O, LSE, s, pl, ws, status, stream);
 }
 
+// ---------------------------------------------------------------- short keys (Nk <= 128)
+template <int D, bool BF16, int NK>
+static int short_ctas_per_sm() {
+  using Cfg = ShortCfg<D, NK>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  static int cache[64];
+  static std::once_flag once[64];
+  std::call_once(once[dev], [&] {
+    cudaFuncSetAttribute(attn_short_kernel<D, BF16, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::kSmemBytes);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_short_kernel<D, BF16, NK>, kShortThreads,
+                                                      Cfg::kSmemBytes) != cudaSuccess)
+      n = 0;
+    cache[dev] = n;
+  });
+  return cache[dev];
+}
+
+template <int D, bool BF16, int NK>
+static attn_status_t launch_short_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                    const Shape &s, int *status, cudaStream_t stream) {
+  ShortParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long zq = static_cast<long long>(s.B) * s.Hq, zk = static_cast<long long>(s.B) * s.Hkv;
+  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16, 64) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16, 64) ||
+      !make_map(&p.tmV, V, D, s.Nk, zk, BF16, 64))
+    return ATTN_ERR_CUDA;
+  p.O = O;
+  p.lse = LSE;
+  p.status = status;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Nq = s.Nq;
+  p.Nk = s.Nk;
+  p.group = s.Hq / s.Hkv;
+  p.causal = s.causal ? 1 : 0;
+  p.window = s.window;
+  p.n_qblocks = (s.Nq + kShortRows - 1) / kShortRows;
+  p.n_units = static_cast<int>(zq * p.n_qblocks);
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  p.timeout_ns = g_timeout_ns.load();
+  const int per_sm = short_ctas_per_sm<D, BF16, NK>(), sms = device_sm_count();
+  if (per_sm <= 0 || sms <= 0) return ATTN_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<long long>(p.n_units, static_cast<long long>(per_sm) * sms));
+  attn_short_kernel<D, BF16, NK><<<grid, kShortThreads, ShortCfg<D, NK>::kSmemBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Shapes with at most 128 keys take the short-key kernel: every head's K and
+// V fit one tile, and the work is bound by moving Q, K, V and O.
+static bool short_path(const Shape &s) {
+  const long long units = static_cast<long long>(s.B) * s.Hq * ((s.Nq + kShortRows - 1) / kShortRows);
+  return s.Nk <= kShortMaxKeys && units <= 0x7fffffffLL;
+}
+
+static attn_status_t dispatch_short(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                    const Shape &s, cudaStream_t stream) {
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
+  const bool nk64 = s.Nk <= 64;
+  if (s.d == 64) {
+    if (nk64)
+      return bf16 ? launch_short_t<64, true, 64>(Q, K, V, O, LSE, s, status, stream)
+                  : launch_short_t<64, false, 64>(Q, K, V, O, LSE, s, status, stream);
+    return bf16 ? launch_short_t<64, true, 128>(Q, K, V, O, LSE, s, status, stream)
+                : launch_short_t<64, false, 128>(Q, K, V, O, LSE, s, status, stream);
+  }
+  if (nk64)
+    return bf16 ? launch_short_t<128, true, 64>(Q, K, V, O, LSE, s, status, stream)
+                : launch_short_t<128, false, 64>(Q, K, V, O, LSE, s, status, stream);
+  return bf16 ? launch_short_t<128, true, 128>(Q, K, V, O, LSE, s, status, stream)
+              : launch_short_t<128, false, 128>(Q, K, V, O, LSE, s, status, stream);
+}
+
 static attn_status_t run(const void *Q, const void *K, const void *V, void *O, float *LSE, const Shape &s,
                          void *ws, size_t ws_bytes, cudaStream_t stream) {
   attn_status_t st = validate(Q, K, V, O, LSE, s);
   if (st != ATTN_OK) return st;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  if (short_path(s)) return dispatch_short(Q, K, V, O, LSE, s, stream);
   if (ws != nullptr) {
     const DecPlan pl = decode_plan(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d);
     if (pl.bytes > 0) {
