@@ -44,7 +44,7 @@ WORKLOAD_TEXT = {
     "mqa_decode": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16",
     "mha_n64_bw": "MHA forward B=512, H=32, N=64, d=64, fp16, causal in {false,true}",
 }
-KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "sm103_ptx.cuh"]
+KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "attn_short.cuh", "sm103_ptx.cuh"]
 
 
 def parse_args():
@@ -193,8 +193,11 @@ def prepare(workload: str, device):
         c["label"] = call_label(shape)
         # split-KV path (decode / few query rows): caller-provided workspace
         wsb = attn.attn_fwd_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d)
-        c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device) if wsb > 0 else None
-        c["kernel"] = "attn_decode_kernel" if wsb > 0 else "attn_fwd_kernel"
+        path = attn.attn_fwd_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d, wsb > 0)
+        c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device) if path == attn.ATTN_PATH_SPLIT_KV else None
+        c["kernel"] = {attn.ATTN_PATH_PREFILL: "attn_fwd_kernel", attn.ATTN_PATH_SPLIT_KV: "attn_decode_kernel",
+                       attn.ATTN_PATH_SHORT: "attn_short_kernel"}[path]
+        c["launches"] = 2 if path == attn.ATTN_PATH_SPLIT_KV else 1  # split kernel + merge kernel
         calls.append(c)
     return calls
 
@@ -484,7 +487,7 @@ def main():
                        "l2": "flushed between timed steps outside the timed events: 256 MiB write, then 256 MiB read",
                        "launch": "one CUDA graph per step", "parallelism": f"replicas x{ws}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": steps * len(calls), "clocks": clocks,
+            "gpu_launches": steps * sum(c["launches"] for c in calls), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -69,6 +69,13 @@ typedef enum {
 
 typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
 
+/* The kernels a call runs (see attn_fwd_ex). */
+typedef enum {
+  ATTN_PATH_PREFILL = 0,  /* tiled tcgen05 kernel: one launch */
+  ATTN_PATH_SPLIT_KV = 1, /* split-KV kernel + merge kernel: two launches */
+  ATTN_PATH_SHORT = 2     /* short-key kernel (Nk <= 128): one launch */
+} attn_path_t;
+
 /* Square attention, Nq = Nk = N.  Equivalent to attn_fwd_ex with Nq = Nk = N
  * and no workspace. */
 attn_status_t attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
@@ -77,6 +84,11 @@ attn_status_t attn_fwd(const void *Q, const void *K, const void *V, void *O, flo
 
 /* General call with Nq query rows against Nk keys (Nq <= Nk when causal; a
  * decode step is Nq = 1 against an Nk-token cache).
+ *
+ * Paths: a call with Nk <= 128 runs the short-key kernel (every head's keys
+ * fit one tile; the workspace, if any, is not used).  Otherwise, when a
+ * workspace is given and the shape qualifies, the split-KV path runs; else
+ * the tiled prefill kernel.  attn_fwd_path() says which.
  *
  * workspace/workspace_bytes: optional DEVICE scratch for the split-KV path
  * (cruxr.ai "FlashDecoding": the keys are split into chunks processed in
@@ -94,6 +106,12 @@ attn_status_t attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, 
  * 32 query rows, i.e. (Hq / Hkv) * Nq <= 32, such as a decode step).  The
  * size depends on the device's SM count, which sets the number of chunks. */
 size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+
+/* The path (attn_path_t) that attn_fwd_ex takes for these sizes on the
+ * current device, with (with_workspace != 0) or without a workspace of
+ * attn_fwd_workspace_bytes(...) bytes; -1 when the sizes are invalid.  Masks,
+ * dtype and scale do not change the path.  No device work. */
+int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace);
 
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O

@@ -20,10 +20,27 @@ def attn():
 
 
 def run_split(attn, shape, q, k, v):
+    """Run the split-KV kernels: through attn_fwd_ex with a workspace where the
+    shape takes that path (Nk > 128), else through attn_fwd_decode_noalloc,
+    which always runs them (attn_fwd_ex sends Nk <= 128 to the short-key
+    kernel)."""
     nbytes = attn.attn_fwd_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d)
-    assert nbytes > 0, "shape should take the split-KV path"
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    return pu.run_cuda(shape, q, k, v, workspace=ws)
+    assert nbytes > 0, "shape should qualify for the split-KV path"
+    path = attn.attn_fwd_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d, True)
+    if path == attn.ATTN_PATH_SPLIT_KV:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        return pu.run_cuda(shape, q, k, v, workspace=ws)
+    assert path == attn.ATTN_PATH_SHORT and shape.Nk <= 128
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((shape.B, shape.Hq, shape.Nq), device="cuda", dtype=torch.float32)
+    code = attn.ATTN_DTYPE_BF16 if shape.dtype == "bf16" else attn.ATTN_DTYPE_FP16
+    st = attn.attn_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                      shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d, shape.causal,
+                                      shape.window, shape.scale, code, torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, attn.attn_status_string(st)
+    assert attn.device_status() == attn.ATTN_OK
+    return o, lse
 
 
 @pytest.mark.parametrize("idx", [0, 1])
@@ -89,3 +106,13 @@ def test_workspace_reuse_is_stateless(attn, oracle_mod):
     o2, l2 = pu.run_cuda(shape, q, k, v, workspace=ws)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     pu.check_full(shape, q, k, v, o1, l1, oracle_mod)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,ws,expect", [
+    (4, 32, 8, 1, 8192, True, 1), (4, 32, 8, 1, 8192, False, 0), (4, 32, 8, 1, 128, True, 2),
+    (2, 4, 4, 64, 64, False, 2), (2, 4, 4, 256, 256, True, 0), (1, 32, 1, 2, 4096, True, 0),
+    (1, 4, 4, 33, 4096, True, 0), (2, 8, 0, 1, 64, False, -1)])
+def test_path_selection(attn, B, Hq, Hkv, Nq, Nk, ws, expect):
+    """attn_fwd_path: short keys first, then split-KV when a workspace is given
+    and the group has at most 32 query rows, else prefill; -1 on bad sizes."""
+    assert attn.attn_fwd_path(B, Hq, Hkv, Nq, Nk, 128, ws) == expect

@@ -25,9 +25,13 @@ ATTN_ERR_SCRATCH_LIMIT = 5
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
+ATTN_PATH_PREFILL = 0
+ATTN_PATH_SPLIT_KV = 1
+ATTN_PATH_SHORT = 2
+
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
-            "attn_fwd_decode_noalloc"]
+            "attn_fwd_decode_noalloc", "attn_fwd_path"]
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.attn_abi_version.restype = ci
         L.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         L.attn_fwd_decode_noalloc.restype = ci
+        L.attn_fwd_path.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+        L.attn_fwd_path.restype = ci
         del fp
         _lib = L
         return _lib
@@ -88,6 +94,10 @@ def attn_fwd_ex(Q, K, V, O, LSE, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale
 
 def attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
     return int(lib().attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d))
+
+
+def attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, with_workspace) -> int:
+    return int(lib().attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, 1 if with_workspace else 0))
 
 
 def attn_fwd_host(Qh, Kh, Vh, Oh, LSEh, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, dev_buf,

@@ -423,6 +423,14 @@ size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   return decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
 }
 
+int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return -1;
+  Shape s{B, Hq, Hkv, Nq, Nk, d, 0, 0, 1.f, ATTN_DTYPE_FP16};
+  if (short_path(s)) return ATTN_PATH_SHORT;
+  if (with_workspace && decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes > 0) return ATTN_PATH_SPLIT_KV;
+  return ATTN_PATH_PREFILL;
+}
+
 static size_t round_up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_lse) {
