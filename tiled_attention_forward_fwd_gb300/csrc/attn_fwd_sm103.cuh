@@ -77,11 +77,22 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barriers: qfull[2][QB], qfree[2][QB], kvfull[NS], kvempty[NS],
-  //           sfull[2], ofinal[2], drain[2]
-  static constexpr int kNumBars = 4 * kQBufs + 2 * kStages + 6;
+  //           sfull[2], ofinal[2], drain[2], pvdone[2]
+  static constexpr int kNumBars = 4 * kQBufs + 2 * kStages + 8;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;
+  // TMEM columns of tile t.  d = 64: S [256t, +128), P [256t + 128, +64) and
+  // O [256t + 192, +64): with P apart from S, the Q K^T of the next key block
+  // can run while the softmax of this one computes P.  d = 128 has no room
+  // for that: P is written over S [128t, +128) and O is [256 + 128t, +128).
+  static constexpr bool kSeparateP = (D == 64);
+  // d = 64 (softmax-bound): exp2 with the running max first, the row max in
+  // the same pass; d = 128 (MMA-bound): max first, then exp2.
+  static constexpr bool kSpeculativeP = (D == 64);
+  static constexpr uint32_t kColS = kSeparateP ? 256 : 128;  // S column stride per tile
+  static constexpr uint32_t kColP = kSeparateP ? 128 : 0;    // P offset within the tile's columns
+  static constexpr uint32_t kColO0 = kSeparateP ? 192 : 256; // O_0
+  static constexpr uint32_t kColOStride = kSeparateP ? 256 : D;
   static constexpr int kThreads = 384;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -187,6 +198,64 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
   return it;
 }
 
+// Row max of a 128-column S row: eight independent chains of 3-input max.
+__device__ __forceinline__ void softmax_rowmax(const uint32_t (&sr)[kBN], float (&mx)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+  for (int c = 8; c < kBN; c += 16) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+  }
+}
+__device__ __forceinline__ float softmax_max8(const float (&mx)[8]) {
+  return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+}
+
+// p = 2^(s * sm_scale * log2 e - m) for the 128 columns of a row, two per
+// packed FMA, written to TMEM as packed 16-bit pairs (32 columns per chunk);
+// rs gets the fp32 sum.  With kMax the row-max chains are updated from the
+// same chunk, so the max costs no extra pass over the row.
+template <bool BF16, bool kMax>
+__device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x2, float m, float2 (&rs)[2],
+                                          float (&mx)[8], uint32_t pcol) {
+  const float mref = (m == -INFINITY) ? 0.f : m;
+  const float2 negm = make_float2(-mref, -mref);
+  rs[0] = rs[1] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int cc = 0; cc < kBN / 32; ++cc) {
+    if constexpr (kMax) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        mx[k] = fmax3(mx[k], __uint_as_float(sr[cc * 32 + k]), __uint_as_float(sr[cc * 32 + 8 + k]));
+        mx[k] = fmax3(mx[k], __uint_as_float(sr[cc * 32 + 16 + k]), __uint_as_float(sr[cc * 32 + 24 + k]));
+      }
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 x = ffma2(make_float2(__uint_as_float(sr[cc * 32 + 2 * i]), __uint_as_float(sr[cc * 32 + 2 * i + 1])),
+                             sl2x2, negm);
+      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      pk[i] = pack2<BF16>(e.x, e.y);
+      rs[i & 1] = fadd2(rs[i & 1], e);
+    }
+    tmem_st16(pcol + cc * 16, pk);
+  }
+}
+
+// Named barriers (id 0 is __syncthreads), each a rendezvous of one softmax
+// warpgroup (128 threads) and its tile's MMA warp (32).
+constexpr uint32_t kBarP = 1, kBarSRead = 3, kBarHandoffThreads = 128 + 32;
+
+// Items are handed to the persistent CTAs in passes of gridDim.x, alternating
+// direction ("snake"): with items sorted longest first, every CTA gets a
+// similar total.  Returns the m-th item of this CTA (>= n_items: none).
+__device__ __forceinline__ int item_of(int m) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return m * g + ((m & 1) ? (g - 1 - c) : c);
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
@@ -210,6 +279,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   auto bSfull = [&](int t) { return bX + 8u * (0 + t); };
   auto bOfinal = [&](int t) { return bX + 8u * (2 + t); };
   auto bDrain = [&](int t) { return bX + 8u * (4 + t); };
+  auto bPVdone = [&](int t) { return bX + 8u * (6 + t); };  // separate-P layout only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -225,6 +295,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       mbar_init(bSfull(t), 1);
       mbar_init(bOfinal(t), 1);
       mbar_init(bDrain(t), 1);
+      mbar_init(bPVdone(t), 1);
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bKVfull(s), 1);
@@ -257,7 +328,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       int nq[2] = {0, 0};
       int ckv = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      for (int mi = 0; ok && mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
+        const int item = item_of(mi);
+        if (item >= p.n_items) continue;
         const Item it = decode_item(p, item);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -304,229 +377,266 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           for (int k = max(0, nq[t] - QB); k < nq[t]; ++k) mbar_drain(bQfull(t, k % QB), (k / QB) & 1);
         for (int c = max(0, ckv - NS); c < ckv; ++c) mbar_drain(bKVfull(c % NS), (c / NS) & 1);
       }
+    } else if (warp >= 2) {
+      // ====================================================== MMA issuer of tile t
+      // One warp per query tile (warps 2 and 3), so that neither tile waits
+      // for the other's issue.  The loop runs on the whole warp; one elected
+      // lane issues each MMA and commit.  Handoffs with the tile's softmax
+      // warpgroup are rendezvous on named barriers:
+      //   kBarP + t       P_t(j) is in TMEM  -> P V of block j may be issued
+      //   kBarSRead + t   S_t(j) is in the softmax registers -> the next
+      //                   Q K^T may overwrite it (separate-P layout only)
+      // Every barrier of the fixed sequence is taken even after a failed
+      // wait, so the partner warpgroup is never left waiting.
+      const int t = warp - 2;
+      int nq = 0;        // items of this tile started (Q buffer use)
+      int ckv = 0;       // ring slots passed
+      int kv_seen = -1;  // last ring slot whose arrival was waited for
+      bool ok = true;
+      // the pending P V: (stage, accumulate, last) of the previous step
+      bool pending = false;
+      int pv_stage = 0;
+      uint32_t pv_acc = 0;
+      bool pv_last = false;
+      auto wait_kv = [&](int c) {
+        if (ok && c > kv_seen) {
+          ok = mbar_wait_warp(bKVfull(c % NS), (c / NS) & 1, wc, kErrWaitKV);
+          kv_seen = c;
+        }
+      };
+      // a ring slot this tile does not read is released once filled (so that
+      // the arrival counts towards this fill, not the last)
+      auto pass_slot = [&](int c) {
+        wait_kv(c);
+        if (ok && elect_one()) umma_commit(bKVempty(c % NS));
+        __syncwarp();
+      };
+      auto issue_qk = [&](int c, int qbuf, bool last) {
+        if (!ok) return;
+        tc_fence_after();
+        const uint64_t qd = sdesc_sw128(sQ + (t * QB + qbuf) * C::kQBytes, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sK + (c % NS) * C::kTileBytes, 16, 1024);
+        if (elect_one()) {
+          mma_qk<D, BF16>(tmem + t * C::kColS, qd, kd);
+          umma_commit(bSfull(t));
+          if (last) umma_commit(bQfree(t, qbuf));
+        }
+        __syncwarp();
+      };
+      auto issue_pv = [&]() {
+        named_bar_sync(kBarP + t, kBarHandoffThreads);
+        ok = ok && *reinterpret_cast<volatile int *>(abort_flag) == 0;
+        if (ok) {
+          tc_fence_after();
+          const uint64_t vd = sdesc_sw128(sV + pv_stage * C::kTileBytes, C::kBoxBytes, 1024);
+          if (elect_one()) {
+            mma_pv<D, BF16>(tmem + C::kColO0 + t * C::kColOStride, tmem + t * C::kColS + C::kColP, vd, pv_acc);
+            umma_commit(bKVempty(pv_stage));
+            if constexpr (C::kSeparateP) umma_commit(bPVdone(t));
+            if (pv_last) umma_commit(bOfinal(t));
+          }
+          __syncwarp();
+        }
+        pending = false;
+      };
+      for (int mi = 0; mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
+        const int item = item_of(mi);
+        if (item >= p.n_items) continue;
+        const Item it = decode_item(p, item);
+        const bool tvalid = t ? it.valid[1] : it.valid[0];
+        const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
+        const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
+        const int c0 = ckv - it.ubeg;  // ring slot of K/V block j is c0 + j
+        for (int j = it.ubeg; j < tbeg; ++j) pass_slot(c0 + j);
+        if (tvalid) {
+          const int qbuf = nq % QB;
+          if (ok) ok = mbar_wait_warp(bQfull(t, qbuf), (nq / QB) & 1, wc, kErrWaitQ);
+          for (int j = tbeg; j < tend; ++j) {
+            const int c = c0 + j;
+            if constexpr (C::kSeparateP) {
+              // S of the previous block read -> Q K^T of block j; then P V of
+              // the previous block once its P is written.
+              if (j > tbeg) named_bar_sync(kBarSRead + t, kBarHandoffThreads);
+              wait_kv(c);
+              issue_qk(c, qbuf, j + 1 == tend);
+              if (pending) issue_pv();
+            } else {
+              // P over S: P V of the previous block must be issued before the
+              // Q K^T that overwrites its P.
+              if (pending) issue_pv();
+              wait_kv(c);
+              issue_qk(c, qbuf, j + 1 == tend);
+            }
+            pending = true;
+            pv_stage = c % NS;
+            pv_acc = (j > tbeg) ? 1u : 0u;
+            pv_last = (j + 1 == tend);
+          }
+          // The item's last P V goes out now: it releases a K/V stage that a
+          // later fill (and this warp's next waits) may need.
+          if constexpr (C::kSeparateP) named_bar_sync(kBarSRead + t, kBarHandoffThreads);
+          issue_pv();
+          nq++;
+        }
+        for (int j = tend; j < it.uend; ++j) pass_slot(c0 + j);
+        ckv = c0 + it.uend;
+      }
+      // Drain every MMA this warp issued before TMEM can be released (the
+      // commit comes from the lane that issued them).
+      if (elect_one()) {
+        umma_commit(bDrain(t));
+        mbar_drain(bDrain(t), 0);
+      }
+      __syncwarp();
     }
     __syncwarp();
   } else {
     regs_inc<kRegsSoftmax>();
-    // ============================================== softmax and MMA issue of tile t
+    // ============================================================== softmax of tile t
     const int t = wg - 1;
     const int quad = warp & 3;
-    const bool issuer = (quad == 0);  // this warp issues the tile's MMAs from one elected lane
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t scol = tmem + lane_off + t * 128;
-    const uint32_t ocol = tmem + lane_off + C::kColO + t * D;
-    const uint32_t named_bar = 1 + t;  // the 4 warps of this warpgroup
+    const uint32_t scol = tmem + lane_off + t * C::kColS;  // S (and P when shared)
+    const uint32_t pcol = scol + C::kColP;                 // P
+    const uint32_t ocol = tmem + lane_off + C::kColO0 + t * C::kColOStride;
     const float sl2 = p.scale_log2;
-    int ns = 0, nfin = 0, nq = 0;
-    int ckv = 0;       // ring slots passed (both tiles walk every slot of every item)
-    int kv_seen = -1;  // last ring slot whose K/V arrival this warp has waited for
-    // `ok` is this thread's view (the issuer warp also fails on its own
-    // waits); `wg_ok` is the warpgroup's, agreed at every named barrier, and
-    // only it decides whether to leave a loop.
-    bool ok = true, wg_ok = true;
-    // issuer warp only: wait until ring slot c holds K_j / V_j
-    auto wait_kv = [&](int c) -> bool {
-      if (c <= kv_seen) return true;
-      if (!mbar_wait_warp(bKVfull(c % NS), (c / NS) & 1, wc, kErrWaitKV)) return false;
-      kv_seen = c;
-      return true;
-    };
-    // issuer warp only: a slot this tile does not read is released as soon as
-    // it is filled (so that the arrival counts towards this fill, not the last)
-    auto pass_slot = [&](int c) -> bool {
-      if (!wait_kv(c)) return false;
-      if (elect_one()) umma_commit(bKVempty(c % NS));
-      __syncwarp();
-      return true;
-    };
-    for (int item = blockIdx.x; wg_ok && item < p.n_items; item += gridDim.x) {
+    int ns = 0, nfin = 0;
+    int npv = 0;  // P V of this tile issued so far (separate P: P_t is reused once the last one is done)
+    bool ok = true;
+    for (int mi = 0; mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
+      const int item = item_of(mi);
+      if (item >= p.n_items) continue;
       const Item it = decode_item(p, item);
       // this warpgroup's tile, as scalars (t is not a compile-time index)
       const bool tvalid = t ? it.valid[1] : it.valid[0];
-      const int trow0 = t ? it.row0[1] : it.row0[0];
-      const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
-      const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
-      const int tbh = t ? it.bh[1] : it.bh[0];
-      const int c0 = ckv - it.ubeg;  // ring slot of K/V tile j is c0 + j
-      const int qbuf = nq % QB;
-      const uint32_t sQt = sQ + (t * QB + qbuf) * C::kQBytes;  // this tile's Q buffer
-      if (issuer) {
-        for (int j = it.ubeg; ok && j < tbeg; ++j) ok = pass_slot(c0 + j);
-        if (ok && tvalid) {
-          // the first S = Q K^T of this tile
-          ok = mbar_wait_warp(bQfull(t, qbuf), (nq / QB) & 1, wc, kErrWaitQ) && wait_kv(c0 + tbeg);
-          if (ok) {
-            tc_fence_after();
-            const uint64_t qd = sdesc_sw128(sQt, 16, 1024);
-            const uint64_t kd = sdesc_sw128(sK + ((c0 + tbeg) % NS) * C::kTileBytes, 16, 1024);
-            if (elect_one()) {
-              mma_qk<D, BF16>(tmem + t * 128, qd, kd);
-              umma_commit(bSfull(t));
-              if (tbeg + 1 == tend) umma_commit(bQfree(t, qbuf));
-            }
-            __syncwarp();
-          }
-        }
-      }
-      ckv = c0 + it.uend;
-      wg_ok = named_bar_and(named_bar, 128, ok);
-      if (!wg_ok) break;
       if (!tvalid) continue;
-      nq++;
+      const int trow0 = t ? it.row0[1] : it.row0[0];
+      const int tbeg = t ? it.beg[1] : it.beg[0];
+      const int tend = t ? it.end[1] : it.end[0];
+      const int tbh = t ? it.bh[1] : it.bh[0];
       const int pos = trow0 + row + (p.Nk - p.Nq);  // absolute position of this query row
       const int p0 = trow0 + (p.Nk - p.Nq);
       const int p1 = min(trow0 + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
       float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
       float l = 0.f;        // running sum of exp2(s * sl2 - m), fp32
       for (int j = tbeg; j < tend; ++j) {
-        // A failed wait still goes through this iteration's barrier, so that
-        // the whole warpgroup leaves together.
+        // After a failed wait the work is skipped but the barriers are not.
         ok = ok && mbar_wait_warp(bSfull(t), ns & 1, wc, kErrWaitS);
+        ns++;
+        uint32_t sr[kBN];
         if (ok) {
-          ns++;
           tc_fence_after();
-          uint32_t sr[kBN];
           tmem_ld128(scol, sr);
+        }
+        if constexpr (C::kSeparateP) {
+          tc_fence_before();
+          named_bar_sync(kBarSRead + t, kBarHandoffThreads);  // S_t(j) read: the next Q K^T may overwrite it
+        }
+        if (ok) {
           const int key0 = j * kBN;
           const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
                                  (p.window > 0 && key0 <= p1 - p.window);
           if (need_mask) {
 #pragma unroll
-            for (int c = 0; c < kBN; ++c)
-              if (!key_live(key0 + c, pos, p.Nk, p.causal, p.window)) sr[c] = 0xff800000u;  // -inf
+            for (int cc = 0; cc < kBN; ++cc)
+              if (!key_live(key0 + cc, pos, p.Nk, p.causal, p.window)) sr[cc] = 0xff800000u;  // -inf
           }
-          // row max: eight independent chains of 3-input max, then a short tree
-          float mx[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) mx[c] = __uint_as_float(sr[c]);
-#pragma unroll
-          for (int c = 8; c < kBN; c += 16) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
-          }
-          const float mxa = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
-          const float m_new = fmaxf(m, mxa * sl2);
-          // Lazy rescale: move the reference max only when it grew by more
-          // than 2^8 somewhere in the warp (the first tile of an item always
-          // sets it).
-          float alpha = 1.f;
           const bool first = (j == tbeg);
-          const bool rescale = !first && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
-          if (first || rescale) {
-            alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-            m = m_new;
+          if constexpr (C::kSeparateP) {
+            // P_t and O_t are free once the P V of block j-1 has completed
+            // (at an item's first block the previous O-final wait covered it).
+            if (!first) ok = mbar_wait_warp(bPVdone(t), (npv - 1) & 1, wc, kErrWaitS);
+            tc_fence_after();
           }
-          const float mref = (m == -INFINITY) ? 0.f : m;
-          // p = 2^(s * sm_scale * log2 e - m), two elements per packed FMA
-          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
-          float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 x = ffma2(make_float2(__uint_as_float(sr[c * 32 + 2 * i]),
-                                                 __uint_as_float(sr[c * 32 + 2 * i + 1])),
-                                     sl2x2, negm);
-              const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              pk[i] = pack2<BF16>(e.x, e.y);
-              rs[i & 1] = fadd2(rs[i & 1], e);
+          const float2 sl2x2 = make_float2(sl2, sl2);
+          float2 rs[2];
+          float mx[8];
+          float alpha = 1.f;
+          bool rescale = false;
+          if (first || !C::kSpeculativeP) {
+            // max first: the first block of an item sets the reference max;
+            // at d = 128 (MMA-bound) every block takes this shorter path
+            softmax_rowmax(sr, mx);
+            const float m_new = fmaxf(m, softmax_max8(mx) * sl2);
+            rescale = !first && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
+            if (first || rescale) {
+              alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+              m = m_new;
             }
-            tmem_st16(scol + c * 16, pk);
+            softmax_p<BF16, false>(sr, sl2x2, m, rs, mx, pcol);
+          } else {
+            // Speculative pass with the current reference max (the row max
+            // is taken in the same pass, off the exp2 critical path); it is
+            // redone only when some row's max grew by more than 2^8 (lazy
+            // rescale), which is rare after an item's first blocks.
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+            softmax_p<BF16, true>(sr, sl2x2, m, rs, mx, pcol);
+            const float m_new = fmaxf(m, softmax_max8(mx) * sl2);
+            rescale = __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
+            if (rescale) {
+              alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+              m = m_new;
+              softmax_p<BF16, false>(sr, sl2x2, m, rs, mx, pcol);
+            }
           }
           l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
           if (rescale) {
-            // S_t(j) is complete, so the P V of tile j-1 (issued before the
-            // QK of tile j, by the same thread, on the in-order tensor pipe)
-            // is too: O_t can be rescaled before the P V of tile j is issued.
+            // O_t holds blocks up to j-1 only: with separate P the P V of
+            // block j-1 was waited for above; with P over S, S_t(j) completing
+            // means that P V (issued before this Q K^T by the same warp, on
+            // the in-order tensor pipe) has too.
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 32; ++cc) {
               uint32_t r[32];
-              tmem_ld32(ocol + c * 32, r);
+              tmem_ld32(ocol + cc * 32, r);
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(ocol + c * 32, r);
+              tmem_st32(ocol + cc * 32, r);
             }
           }
           tmem_st_wait();
-          tc_fence_before();
         }
-        wg_ok = named_bar_and(named_bar, 128, ok);  // P_t(j) (and O_t) written by all four warps
-        if (!wg_ok) break;
-        if (issuer) {
-          const int c = c0 + j;
-          const bool more = (j + 1 < tend);
-          // Wait for the next K/V before issuing anything: with none of our
-          // MMAs in flight the check is cheap.
-          if (more) ok = wait_kv(c + 1);
-          if (ok) {
-            tc_fence_after();
-            const uint64_t vd = sdesc_sw128(sV + (c % NS) * C::kTileBytes, C::kBoxBytes, 1024);
-            const uint64_t qd = sdesc_sw128(sQt, 16, 1024);
-            const uint64_t kd = sdesc_sw128(sK + ((c + 1) % NS) * C::kTileBytes, 16, 1024);
-            const uint32_t acc = (j > tbeg) ? 1u : 0u;
-            if (elect_one()) {
-              mma_pv<D, BF16>(tmem + C::kColO + t * D, tmem + t * 128, vd, acc);
-              umma_commit(bKVempty(c % NS));
-              if (more) {
-                mma_qk<D, BF16>(tmem + t * 128, qd, kd);
-                umma_commit(bSfull(t));
-                if (j + 2 == tend) umma_commit(bQfree(t, qbuf));
-              } else {
-                umma_commit(bOfinal(t));
-              }
-            }
-            __syncwarp();
-          }
-        }
+        tc_fence_before();
+        named_bar_sync(kBarP + t, kBarHandoffThreads);  // P_t(j) (and O_t) written: P V of block j may go
+        npv++;
       }
-      if (!wg_ok) break;
-      if (issuer)
-        for (int j = tend; ok && j < it.uend; ++j) ok = pass_slot(c0 + j);
       // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2
       ok = ok && mbar_wait_warp(bOfinal(t), nfin & 1, wc, kErrWaitOFinal);
-      wg_ok = named_bar_and(named_bar, 128, ok);
-      if (!wg_ok) break;
       nfin++;
-      tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      const int grow = trow0 + row;
-      const bool live_row = grow < p.Nq;
-      uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                      (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
+      if (ok) {
+        tc_fence_after();
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const int grow = trow0 + row;
+        const bool live_row = grow < p.Nq;
+        uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                        (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(ocol + c * 32, r);
-        if (live_row) {
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(ocol + cc * 32, r);
+          if (live_row) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv);
-            w.y = pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv);
-            w.z = pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
-            w.w = pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
-            *reinterpret_cast<uint4 *>(orow + c * 64 + q * 16) = w;
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv);
+              w.y = pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv);
+              w.z = pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
+              w.w = pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
+              *reinterpret_cast<uint4 *>(orow + cc * 64 + q * 16) = w;
+            }
           }
         }
+        if (live_row && p.lse != nullptr)
+          p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
+              ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
       }
       // The next item's first P V (accumulate = 0) overwrites O_t; it is
-      // issued after a named barrier that every warp reaches only after this
-      // read has completed (tcgen05.ld waits for its data).
+      // issued only after the next P barrier, which these warps reach after
+      // this read has completed (tcgen05.ld waits for its data).
       tc_fence_before();
-      if (live_row && p.lse != nullptr)
-        p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
-            ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
     }
-    // Never release TMEM with one of our MMAs in flight: the commit comes from
-    // the lane that issued them.
-    if (issuer && elect_one()) {
-      umma_commit(bDrain(t));
-      mbar_drain(bDrain(t), 0);
-    }
-    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();

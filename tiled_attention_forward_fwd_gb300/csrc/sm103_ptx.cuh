@@ -35,6 +35,11 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32) that
 // also returns the AND of `v` over them: every participant gets the same
 // answer, so a decision to leave a loop stays uniform and no thread is left
