@@ -90,6 +90,13 @@ static int current_device_sm_major(int *dev_out) {
   return major;
 }
 
+static int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 template <int D, bool BF16>
 static attn_status_t launch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                    const Shape &s, cudaStream_t stream) {
@@ -114,12 +121,28 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.group = s.Hq / s.Hkv;
   p.causal = s.causal ? 1 : 0;
   p.window = s.window;
-  // An item holds two query tiles: two heads of one GQA group at the same
-  // rows when the group size is even, else two consecutive row tiles.
-  p.heads_mode = (p.group % 2 == 0) ? 1 : 0;
-  const int rows_per_item = p.heads_mode ? kBM : 2 * kBM;
-  p.n_row_blocks = (s.Nq + rows_per_item - 1) / rows_per_item;
-  const long long slots = p.heads_mode ? zq / 2 : zq;
+  // An item holds up to two query tiles: two heads of one GQA group at the
+  // same rows when the group size is even (they share every K/V load);
+  // otherwise row tiles of one head, paired so that the longest item is as
+  // short as possible: one tile per item when every tile can have an SM,
+  // mirrored pairs (r, n-1-r) for a causal call that fits one wave,
+  // consecutive pairs (2r, 2r+1) otherwise.
+  const int sms_now = device_sm_count();
+  const long long ntiles = (s.Nq + kBM - 1) / kBM;
+  if (p.group % 2 == 0) {
+    p.pair_mode = kPairHeads;
+    p.n_row_blocks = static_cast<int>(ntiles);
+  } else if (zq * ntiles <= sms_now) {
+    p.pair_mode = kPairSingle;
+    p.n_row_blocks = static_cast<int>(ntiles);
+  } else if (s.causal && zq * ((ntiles + 1) / 2) <= sms_now) {
+    p.pair_mode = kPairMirror;
+    p.n_row_blocks = static_cast<int>((ntiles + 1) / 2);
+  } else {
+    p.pair_mode = kPairRows;
+    p.n_row_blocks = static_cast<int>((ntiles + 1) / 2);
+  }
+  const long long slots = (p.pair_mode == kPairHeads) ? zq / 2 : zq;
   const long long items = slots * p.n_row_blocks;
   if (items > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   p.n_slots = static_cast<int>(slots);
@@ -162,12 +185,6 @@ struct DecPlan {
   size_t bytes = 0;  // 0: this shape does not take the split-KV path
 };
 
-static int device_sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
 
 // Resident CTAs per SM of the split kernel for (d, row blocks), from the
 // occupancy calculator (shared memory and registers decide it).

@@ -57,9 +57,9 @@ struct FwdParams {
   int *status;      // device status word
   int B, Hq, Hkv, Nq, Nk, group;
   int causal, window;
-  int heads_mode;    // 1: item = heads (h, h+1) at the same 128 rows; 0: rows (r, r+128) of one head
-  int n_row_blocks;  // row blocks per (b, head slot)
-  int n_slots;       // heads_mode ? B*Hq/2 : B*Hq
+  int pair_mode;     // how an item's two query tiles are chosen (kPair*)
+  int n_row_blocks;  // items per (b, head slot)
+  int n_slots;       // pair_mode == kPairHeads ? B*Hq/2 : B*Hq
   int n_items;
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
@@ -163,11 +163,22 @@ __device__ __forceinline__ void tile_range(const FwdParams &p, int row0, int &be
   }
 }
 
+// Item shapes (the host picks one per call):
+//   kPairHeads   two query heads of one GQA group at the same 128 rows: each
+//                K/V tile load serves both (group size even)
+//   kPairRows    row tiles 2r and 2r+1 of one head (the default otherwise)
+//   kPairMirror  row tiles r and n-1-r of one head: with a causal mask the
+//                two lengths add up to about the same for every item, which
+//                shortens the longest item when all items run in one wave
+//   kPairSingle  one row tile per item: when every tile can have its own SM
+enum PairMode : int { kPairRows = 0, kPairHeads = 1, kPairMirror = 2, kPairSingle = 3 };
+
 __device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
   Item it;
-  const int rb = p.n_row_blocks - 1 - item / p.n_slots;  // longest (last) row blocks first
+  const int idx = item / p.n_slots;  // longest items first
   const int slot = item % p.n_slots;
-  if (p.heads_mode) {
+  if (p.pair_mode == kPairHeads) {
+    const int rb = p.n_row_blocks - 1 - idx;
     const int hp = p.Hq / 2;
     it.b = slot / hp;
     const int h0 = (slot % hp) * 2;
@@ -180,8 +191,19 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
     const int h = slot % p.Hq;
     it.bh[0] = it.bh[1] = slot;
     it.kvh = h / p.group;
-    it.row0[0] = rb * 2 * kBM;
-    it.row0[1] = rb * 2 * kBM + kBM;
+    if (p.pair_mode == kPairRows) {
+      const int rb = p.n_row_blocks - 1 - idx;
+      it.row0[0] = rb * 2 * kBM;
+      it.row0[1] = rb * 2 * kBM + kBM;
+    } else if (p.pair_mode == kPairMirror) {
+      const int ntiles = (p.Nq + kBM - 1) / kBM;
+      const int a = idx, c = ntiles - 1 - idx;  // a <= c
+      it.row0[0] = a * kBM;
+      it.row0[1] = (c > a) ? c * kBM : p.Nq;  // the middle tile of an odd count goes alone
+    } else {
+      it.row0[0] = (p.n_row_blocks - 1 - idx) * kBM;
+      it.row0[1] = p.Nq;  // no second tile
+    }
   }
   it.ubeg = 1 << 30;
   it.uend = 0;
