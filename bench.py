@@ -222,9 +222,13 @@ def make_event():
         return torch.cuda.Event(enable_timing=True)
 
 
-def build_graph(calls, stream):
-    """Capture one step (every call, with a timing event between launches)."""
-    evs = [make_event() for _ in range(len(calls) + 1)]
+def build_graph(calls, stream, per_call_events: bool):
+    """Capture one step (every call, back to back).  With per_call_events a
+    timing event sits between launches; that graph gives the per-call times,
+    but an event between two kernels also keeps the second from starting its
+    prologue early (programmatic dependent launch), so the step time comes
+    from the graph without them."""
+    evs = [make_event() for _ in range(len(calls) + 1)] if per_call_events else []
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         # warm the launch path (tensor-map encoder, kernel attributes) before capture
@@ -232,10 +236,12 @@ def build_graph(calls, stream):
             launch(c, stream.cuda_stream)
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
-            evs[0].record(stream)
+            if per_call_events:
+                evs[0].record(stream)
             for i, c in enumerate(calls):
                 launch(c, stream.cuda_stream)
-                evs[i + 1].record(stream)
+                if per_call_events:
+                    evs[i + 1].record(stream)
     return g, evs
 
 
@@ -249,12 +255,15 @@ def device_timing(calls, steps, warmup, device, stream):
         flush.fill_(1.0)  # evicts everything (larger than the 129 MB L2) ...
         flush_rd.sum()    # ... and this read leaves only clean lines behind
 
-    g, evs = build_graph(calls, stream)
+    g, _ = build_graph(calls, stream, per_call_events=False)
+    g_calls, evs = build_graph(calls, stream, per_call_events=True)
     t_start, t_stop = make_event(), make_event()
     for _ in range(warmup):
         with torch.cuda.stream(stream):
             flush_l2()
-        g.replay()
+            g.replay()
+            flush_l2()
+            g_calls.replay()
     torch.cuda.synchronize(device)
     step_ms, call_ms = [], [[] for _ in calls]
     for _ in range(steps):
@@ -265,6 +274,12 @@ def device_timing(calls, steps, warmup, device, stream):
             t_stop.record(stream)
         stream.synchronize()
         step_ms.append(t_start.elapsed_time(t_stop))
+    # per-call device times (the roofline's dominant call), same flush
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush_l2()
+            g_calls.replay()
+        stream.synchronize()
         for i in range(len(calls)):
             call_ms[i].append(evs[i].elapsed_time(evs[i + 1]))
     st = attn.attn_device_status(stream.cuda_stream)
@@ -485,7 +500,8 @@ def main():
                        "calls_per_step": len(calls),
                        "flop_convention": "4*B*Hq*N^2*d, halved for square causal; exact live pairs otherwise",
                        "l2": "flushed between timed steps outside the timed events: 256 MiB write, then 256 MiB read",
-                       "launch": "one CUDA graph per step", "parallelism": f"replicas x{ws}"},
+                       "launch": "one CUDA graph per step (per-call times from a second graph with events between calls)",
+                       "parallelism": f"replicas x{ws}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": steps * sum(c["launches"] for c in calls), "clocks": clocks,
         }

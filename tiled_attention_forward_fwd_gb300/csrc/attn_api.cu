@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "../../include/attn.h"
 #include "attn_decode.cuh"
@@ -54,6 +55,26 @@ static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long
                    const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream finishes; it waits (griddepcontrol.wait)
+// before touching global memory.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -166,7 +187,8 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   });
   if (!regs_ok[dev] || n_sms[dev] <= 0) return ATTN_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(std::min<long long>(items, n_sms[dev]));
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
+  if (launch_pdl(kern, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -283,11 +305,10 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   // (the plan already set the shared-memory attribute of both kernels)
   if (decode_ctas_per_sm(D, p.R <= 16 ? 1 : 2) <= 0) return ATTN_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(zk));
-  if (p.R <= 16)
-    attn_decode_kernel<D, BF16, 1><<<grid, kDecThreads, DecCfg<D, 1>::kSmemBytes, stream>>>(p);
-  else
-    attn_decode_kernel<D, BF16, 2><<<grid, kDecThreads, DecCfg<D, 2>::kSmemBytes, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaError_t le =
+      (p.R <= 16) ? launch_pdl(attn_decode_kernel<D, BF16, 1>, grid, dim3(kDecThreads), DecCfg<D, 1>::kSmemBytes, stream, p)
+                  : launch_pdl(attn_decode_kernel<D, BF16, 2>, grid, dim3(kDecThreads), DecCfg<D, 2>::kSmemBytes, stream, p);
+  if (le != cudaSuccess || cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   // The merge kernel is a programmatic dependent: it may launch while the
   // split kernel runs and waits (griddepcontrol.wait) for its results.
   const int rows = s.B * s.Hq * s.Nq;
@@ -368,7 +389,9 @@ static attn_status_t launch_short_t(const void *Q, const void *K, const void *V,
   const int per_sm = short_ctas_per_sm<D, BF16, NK>(), sms = device_sm_count();
   if (per_sm <= 0 || sms <= 0) return ATTN_ERR_CUDA;
   const int grid = static_cast<int>(std::min<long long>(p.n_units, static_cast<long long>(per_sm) * sms));
-  attn_short_kernel<D, BF16, NK><<<grid, kShortThreads, ShortCfg<D, NK>::kSmemBytes, stream>>>(p);
+  if (launch_pdl(attn_short_kernel<D, BF16, NK>, dim3(grid), dim3(kShortThreads), ShortCfg<D, NK>::kSmemBytes,
+                 stream, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
 
   // Let the merge kernel launch now; it waits for this grid to finish
   // before it reads anything.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // inputs may come from the previous kernel on the stream
   bool ok = true;
 
   if (warp == kDecWarps) {
@@ -434,8 +435,10 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const float *w
   extern __shared__ float wts[];  // [nchunks] weights, then [groups][D] partial sums
   __shared__ float red[4];
   // Launched as a programmatic dependent of the split kernel: wait until it
-  // has finished and its writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // has finished and its writes are visible; the next call may start its
+  // prologue meanwhile.
+  pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.x;
   if (row >= rows) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

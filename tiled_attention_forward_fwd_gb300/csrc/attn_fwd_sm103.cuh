@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+  pdl_launch_dependents();  // the next call's prologue may overlap this one
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // inputs may come from the previous kernel on the stream
   const uint32_t tmem = *tmem_slot;
   const int wg = warp >> 2;
 

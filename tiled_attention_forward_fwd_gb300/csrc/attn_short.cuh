@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kShortThreads, ShortCfg<D, NK>::kMinCtas)
   auto bEmpty = [&](int s) { return bar0 + 8u * (NS + s); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+  pdl_launch_dependents();  // the next call's prologue may overlap this one
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kShortThreads, ShortCfg<D, NK>::kMinCtas)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // inputs may come from the previous kernel on the stream
   bool ok = true;
 
   if (warp == kShortWarps) {

@@ -56,6 +56,16 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
   return r != 0;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream (when launched with programmatic serialization) start its
+// prologue now; pdl_wait blocks until every prerequisite grid has completed
+// and its memory is visible.  A kernel calls pdl_wait before its first
+// global-memory access; without programmatic serialization both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
