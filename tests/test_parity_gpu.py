@@ -90,6 +90,35 @@ def test_rescale_stress(attn, oracle_mod, d, key_scale):
     pu.check_full(shape, q, k, v, o, lse, oracle_mod, "rescale stress")
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("kind,x", [("step", 0.5), ("step", 1.5), ("step", 3.0), ("spike", 7.5)])
+def test_rescale_triggers(attn, oracle_mod, dtype, kind, x):
+    """Scores set per K/V tile of 128 keys, so that the decision to rescale is
+    taken exactly at the lazy-rescale threshold.  "stepX": every key of tile b
+    scores b*X (log2 units, row 0); the running sum of a tile then exceeds
+    2^8 once the max has grown by more than 1, although the max grows by less
+    than 8 per tile.  "spikeX": one key per tile scores b*X, the others far
+    below; p reaches 2^7.5 without a rescale on odd tiles and forces one on
+    even tiles.  Row i scales every score by 1 + (i % 7) / 7."""
+    N, d = 2048, 64
+    shape = ai.AttnShape(1, 2, 2, N, N, d, dtype, False)
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    ln2 = float(np.log(2.0))
+    blk = torch.arange(N, dtype=torch.float64) // 128
+    c = blk * x * ln2  # natural-log units; d^-1/2 * q0 = 1 below
+    if kind == "spike":
+        c = torch.where(torch.arange(N) % 128 == 5, c, torch.full_like(c, -30.0))
+    q = torch.zeros(1, 2, N, d, dtype=torch.float64)
+    q[..., 0] = 8.0 * (1.0 + (torch.arange(N) % 7) / 7.0)
+    k = torch.zeros(1, 2, N, d, dtype=torch.float64)
+    k[..., 0] = c
+    k[..., 1:] = ai.normal_tensor(84, (1, 2, N, d - 1), "f64") * 0.01
+    v = ai.normal_tensor(85, (1, 2, N, d), "f64")
+    q, k, v = q.to(tdt), k.to(tdt), v.to(tdt)
+    o, lse = pu.run_cuda(shape, q, k, v)
+    pu.check_full(shape, q, k, v, o, lse, oracle_mod, f"rescale triggers {kind} {x}")
+
+
 def test_lse_optional_and_streams(attn, oracle_mod):
     shape = ai.AttnShape(2, 4, 4, 333, 333, 64, "fp16", True)
     q, k, v = ai.make_qkv(shape, config_id=56)

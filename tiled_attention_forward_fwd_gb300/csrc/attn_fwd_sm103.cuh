@@ -38,6 +38,7 @@ namespace attn {
 constexpr int kBM = 128;  // query rows per tile (tcgen05 M)
 constexpr int kBN = 128;  // keys per K/V tile (MMA N of S, MMA K of P V)
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold: a factor 256
+constexpr float kRescaleSum = 256.0f;  // 2^kRescaleLog2
 
 enum DeviceError : int {
   kErrWaitQ = 0x101,
@@ -220,12 +221,14 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
   return it;
 }
 
-// Row max of a 128-column S row: eight independent chains of 3-input max.
+// Row max of a 128-column S row: eight independent chains, columns 0-15 by
+// a 2-input max, then 16 columns per 3-input max step.
 __device__ __forceinline__ void softmax_rowmax(const uint32_t (&sr)[kBN], float (&mx)[8]) {
+  static_assert(kBN % 16 == 0, "16 columns per step");
 #pragma unroll
-  for (int c = 0; c < 8; ++c) mx[c] = __uint_as_float(sr[c]);
+  for (int k = 0; k < 8; ++k) mx[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
 #pragma unroll
-  for (int c = 8; c < kBN; c += 16) {
+  for (int c = 16; c < kBN; c += 16) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
   }
@@ -236,23 +239,15 @@ __device__ __forceinline__ float softmax_max8(const float (&mx)[8]) {
 
 // p = 2^(s * sm_scale * log2 e - m) for the 128 columns of a row, two per
 // packed FMA, written to TMEM as packed 16-bit pairs (32 columns per chunk);
-// rs gets the fp32 sum.  With kMax the row-max chains are updated from the
-// same chunk, so the max costs no extra pass over the row.
-template <bool BF16, bool kMax>
+// rs gets the fp32 sum.
+template <bool BF16>
 __device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x2, float m, float2 (&rs)[2],
-                                          float (&mx)[8], uint32_t pcol) {
+                                          uint32_t pcol) {
   const float mref = (m == -INFINITY) ? 0.f : m;
   const float2 negm = make_float2(-mref, -mref);
   rs[0] = rs[1] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int cc = 0; cc < kBN / 32; ++cc) {
-    if constexpr (kMax) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        mx[k] = fmax3(mx[k], __uint_as_float(sr[cc * 32 + k]), __uint_as_float(sr[cc * 32 + 8 + k]));
-        mx[k] = fmax3(mx[k], __uint_as_float(sr[cc * 32 + 16 + k]), __uint_as_float(sr[cc * 32 + 24 + k]));
-      }
-    }
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -266,8 +261,8 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x
   }
 }
 
-// Named barriers (id 0 is __syncthreads), each a rendezvous of one softmax
-// warpgroup (128 threads) and its tile's MMA warp (32).
+// Named barriers (id 0 is __syncthreads), each between one softmax warpgroup
+// (128 threads, which only arrive) and its tile's MMA warp (32, which waits).
 constexpr uint32_t kBarP = 1, kBarSRead = 3, kBarHandoffThreads = 128 + 32;
 
 // Items are handed to the persistent CTAs in passes of gridDim.x, alternating
@@ -405,13 +400,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       // ====================================================== MMA issuer of tile t
       // One warp per query tile (warps 2 and 3), so that neither tile waits
       // for the other's issue.  The loop runs on the whole warp; one elected
-      // lane issues each MMA and commit.  Handoffs with the tile's softmax
-      // warpgroup are rendezvous on named barriers:
+      // lane issues each MMA and commit.  Handoffs from the tile's softmax
+      // warpgroup are named barriers that the warpgroup arrives at (without
+      // waiting) and this warp syncs on:
       //   kBarP + t       P_t(j) is in TMEM  -> P V of block j may be issued
       //   kBarSRead + t   S_t(j) is in the softmax registers -> the next
       //                   Q K^T may overwrite it (separate-P layout only)
-      // Every barrier of the fixed sequence is taken even after a failed
-      // wait, so the partner warpgroup is never left waiting.
+      // An arrival never meets the previous use of its barrier still open:
+      // the warpgroup arrives for block j+1 only after waiting for S_t(j+1)
+      // (and, with separate P, for P V of block j), which this warp issues
+      // after its syncs for block j.  Every barrier of the fixed sequence is
+      // taken even after a failed wait, so this warp is never left waiting.
       const int t = warp - 2;
       int nq = 0;        // items of this tile started (Q buffer use)
       int ckv = 0;       // ring slots passed
@@ -555,7 +554,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         }
         if constexpr (C::kSeparateP) {
           tc_fence_before();
-          named_bar_sync(kBarSRead + t, kBarHandoffThreads);  // S_t(j) read: the next Q K^T may overwrite it
+          named_bar_arrive(kBarSRead + t, kBarHandoffThreads);  // S_t(j) read: the next Q K^T may overwrite it
         }
         if (ok) {
           const int key0 = j * kBN;
@@ -588,21 +587,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
               alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
               m = m_new;
             }
-            softmax_p<BF16, false>(sr, sl2x2, m, rs, mx, pcol);
+            softmax_p<BF16>(sr, sl2x2, m, rs, pcol);
           } else {
-            // Speculative pass with the current reference max (the row max
-            // is taken in the same pass, off the exp2 critical path); it is
-            // redone only when some row's max grew by more than 2^8 (lazy
-            // rescale), which is rare after an item's first blocks.
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-            softmax_p<BF16, true>(sr, sl2x2, m, rs, mx, pcol);
-            const float m_new = fmaxf(m, softmax_max8(mx) * sl2);
-            rescale = __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
+            // Speculative pass with the current reference max, no row max.
+            // No p exceeds the row sum, so a sum of at most 2^8 shows that
+            // the max grew by at most 8 (log2 domain) and the pass stands
+            // (lazy rescale).  Otherwise, or while the row has no finite max
+            // yet, the row max is taken and the pass redone; after an item's
+            // first blocks that is rare.
+            softmax_p<BF16>(sr, sl2x2, m, rs, pcol);
+            const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
+            rescale = __any_sync(0xffffffffu, !(rsum <= kRescaleSum) || m == -INFINITY);
             if (rescale) {
+              softmax_rowmax(sr, mx);
+              const float m_new = fmaxf(m, softmax_max8(mx) * sl2);
               alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
               m = m_new;
-              softmax_p<BF16, false>(sr, sl2x2, m, rs, mx, pcol);
+              softmax_p<BF16>(sr, sl2x2, m, rs, pcol);
             }
           }
           l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           tmem_st_wait();
         }
         tc_fence_before();
-        named_bar_sync(kBarP + t, kBarHandoffThreads);  // P_t(j) (and O_t) written: P V of block j may go
+        named_bar_arrive(kBarP + t, kBarHandoffThreads);  // P_t(j) (and O_t) written: P V of block j may go
         npv++;
       }
       // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2

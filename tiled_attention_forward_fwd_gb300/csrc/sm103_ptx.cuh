@@ -35,6 +35,14 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Arrival at named barrier `id` (1..15, over `count` threads, a multiple of
+// 32) without waiting for it to complete; the barrier completes once `count`
+// threads have arrived or synced, and memory accesses before the arrival are
+// then visible to the threads that synced.  The arriving side must not reach
+// the same barrier again before that completion.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
