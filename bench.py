@@ -44,7 +44,7 @@ WORKLOAD_TEXT = {
     "mqa_decode": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16",
     "mha_n64_bw": "MHA forward B=512, H=32, N=64, d=64, fp16, causal in {false,true}",
 }
-KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "attn_short.cuh", "sm103_ptx.cuh"]
+KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "attn_short.cuh", "sm103_ptx.cuh", "fastdiv.h"]
 
 
 def parse_args():

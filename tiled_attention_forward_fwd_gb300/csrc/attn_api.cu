@@ -127,7 +127,7 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   const long long zq = static_cast<long long>(s.B) * s.Hq;
   const long long zk = static_cast<long long>(s.B) * s.Hkv;
   if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16) ||
-      !make_map(&p.tmV, V, D, s.Nk, zk, BF16))
+      !make_map(&p.tmV, V, D, s.Nk, zk, BF16) || (Cfg::kStoreOViaSmem && !make_map(&p.tmO, O, D, s.Nq, zq, BF16)))
     return ATTN_ERR_CUDA;
   int *status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -168,6 +168,9 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   if (items > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   p.n_slots = static_cast<int>(slots);
   p.n_items = static_cast<int>(items);
+  p.fd_slots = fastdiv_make(static_cast<uint32_t>(p.n_slots));
+  p.fd_heads = fastdiv_make(static_cast<uint32_t>(p.pair_mode == kPairHeads ? s.Hq / 2 : s.Hq));
+  p.fd_group = fastdiv_make(static_cast<uint32_t>(p.group));
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
 

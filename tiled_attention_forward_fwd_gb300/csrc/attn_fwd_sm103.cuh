@@ -7,30 +7,31 @@
 // row; O / l and the log-sum-exp m + log l stored at the end).
 //
 // GB300 mapping.  A persistent grid (one CTA per SM) walks a static list of
-// work items, longest first.  An item is two 128-row query tiles that read
-// the same K/V rows: two heads of one GQA group at the same rows when the
-// group size is even (each K/V tile load then serves both heads), else two
-// consecutive row tiles of one head.  12 warps in three warpgroups:
+// work items, longest first, in passes that alternate direction.  An item is
+// up to two 128-row query tiles that read the same K/V rows (two heads of one
+// GQA group at the same rows, or two row tiles of one head; the host picks
+// the pairing per call).  12 warps in three warpgroups:
 //   WG0  warp 0: TMA producer -- Q tiles, then K_j / V_j into an NS-stage
 //                shared-memory ring (128B-swizzled boxes of 128 rows x 64 cols;
 //                K_j and V_j complete one barrier)
-//        warp 1: owns TMEM (512 columns) and issues tcgen05.mma from one
+//        warp 1: owns TMEM (512 columns: allocation and release)
+//        warps 2, 3: MMA issuer of tile 0 / tile 1, tcgen05.mma from one
 //                elected lane of the converged warp:
 //                  S_t = Q_t K_j^T  (A, B in shared memory, fp32 in TMEM)
 //                  O_t += P_t V_j   (A = P_t in TMEM, B = V_j in shared memory)
-//                alternating between the two tiles so that one tile's
-//                contractions run while the other tile's softmax runs
 //   WG1, WG2     softmax of tile 0 / tile 1: thread r owns query row r (TMEM
 //                lane r); loads its S row, masks, keeps the running max and
-//                sums in the log2 domain (sm_scale folded into log2 e), writes
-//                P as packed 16-bit pairs over the S columns, and rescales its
-//                O row in TMEM only when the running max grew by more than 2^8;
-//                after an item's last tile it reads O_t, frees it for the next
-//                item and writes O / l (16-bit) and LSE to global memory
-// TMEM columns: S/P of tile t at [128 t, 128 t + 128), O_t at 256 + t*D.
+//                sum in the log2 domain (sm_scale folded into log2 e), writes
+//                P as packed 16-bit pairs to TMEM, and rescales its O row in
+//                TMEM only when the running max grew by more than 2^8; after
+//                an item's last K/V tile it writes O / l (16-bit) and the LSE.
+// The softmax warpgroup hands S-read and P-written to its MMA warp on named
+// barriers; the MMA warp signals S ready, P V done and O final on mbarriers
+// through tcgen05.commit.  TMEM layout and epilogue per head dim: FwdCfg.
 // Every mbarrier wait is bounded (see sm103_ptx.cuh).
 #pragma once
 
+#include "fastdiv.h"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -53,6 +54,7 @@ struct FwdParams {
   CUtensorMap tmQ;  // (d, Nq, B*Hq)
   CUtensorMap tmK;  // (d, Nk, B*Hkv)
   CUtensorMap tmV;  // (d, Nk, B*Hkv)
+  CUtensorMap tmO;  // (d, Nq, B*Hq): tile stores of O (d = 64)
   void *O;          // (B*Hq*Nq, d) 16-bit
   float *lse;       // (B*Hq*Nq) or null
   int *status;      // device status word
@@ -62,6 +64,9 @@ struct FwdParams {
   int n_row_blocks;  // items per (b, head slot)
   int n_slots;       // pair_mode == kPairHeads ? B*Hq/2 : B*Hq
   int n_items;
+  FastDiv fd_slots;  // / n_slots
+  FastDiv fd_heads;  // / (pair_mode == kPairHeads ? Hq/2 : Hq): the head slots of one batch
+  FastDiv fd_group;  // / group
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
 };
@@ -87,9 +92,15 @@ struct FwdCfg {
   // can run while the softmax of this one computes P.  d = 128 has no room
   // for that: P is written over S [128t, +128) and O is [256 + 128t, +128).
   static constexpr bool kSeparateP = (D == 64);
-  // d = 64 (softmax-bound): exp2 with the running max first, the row max in
-  // the same pass; d = 128 (MMA-bound): max first, then exp2.
+  // d = 64 (softmax-bound): exp2 with the running max first, the row max
+  // only when the row sum shows that the max grew past the lazy-rescale
+  // threshold; d = 128 (MMA-bound): max first, then exp2.
   static constexpr bool kSpeculativeP = (D == 64);
+  // d = 64: the epilogue stages the O tile in the item's Q buffer (free once
+  // the tile's last Q K^T is done) and writes it with one TMA store; the
+  // softmax warpgroup, not the MMA warp, then releases the Q buffer.  d = 128
+  // (one Q buffer per tile, long items) stores rows from registers.
+  static constexpr bool kStoreOViaSmem = (D == 64);
   static constexpr uint32_t kColS = kSeparateP ? 256 : 128;  // S column stride per tile
   static constexpr uint32_t kColP = kSeparateP ? 128 : 0;    // P offset within the tile's columns
   static constexpr uint32_t kColO0 = kSeparateP ? 192 : 256; // O_0
@@ -176,22 +187,19 @@ enum PairMode : int { kPairRows = 0, kPairHeads = 1, kPairMirror = 2, kPairSingl
 
 __device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
   Item it;
-  const int idx = item / p.n_slots;  // longest items first
-  const int slot = item % p.n_slots;
+  int idx, slot, hs;
+  fastdiv_divmod(p.fd_slots, item, idx, slot);  // idx: longest items first
+  fastdiv_divmod(p.fd_heads, slot, it.b, hs);
   if (p.pair_mode == kPairHeads) {
     const int rb = p.n_row_blocks - 1 - idx;
-    const int hp = p.Hq / 2;
-    it.b = slot / hp;
-    const int h0 = (slot % hp) * 2;
+    const int h0 = hs * 2;
     it.bh[0] = it.b * p.Hq + h0;
     it.bh[1] = it.bh[0] + 1;
-    it.kvh = h0 / p.group;
+    it.kvh = static_cast<int>(fastdiv_div(p.fd_group, h0));
     it.row0[0] = it.row0[1] = rb * kBM;
   } else {
-    it.b = slot / p.Hq;
-    const int h = slot % p.Hq;
     it.bh[0] = it.bh[1] = slot;
-    it.kvh = h / p.group;
+    it.kvh = static_cast<int>(fastdiv_div(p.fd_group, hs));
     if (p.pair_mode == kPairRows) {
       const int rb = p.n_row_blocks - 1 - idx;
       it.row0[0] = rb * 2 * kBM;
@@ -264,6 +272,8 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x
 // Named barriers (id 0 is __syncthreads), each between one softmax warpgroup
 // (128 threads, which only arrive) and its tile's MMA warp (32, which waits).
 constexpr uint32_t kBarP = 1, kBarSRead = 3, kBarHandoffThreads = 128 + 32;
+// Named barrier of one softmax warpgroup alone: its O tile is staged.
+constexpr uint32_t kBarOStaged = 5;
 
 // Items are handed to the persistent CTAs in passes of gridDim.x, alternating
 // direction ("snake"): with items sorted longest first, every CTA gets a
@@ -342,6 +352,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         tma_prefetch_desc(&p.tmQ);
         tma_prefetch_desc(&p.tmK);
         tma_prefetch_desc(&p.tmV);
+        if (C::kStoreOViaSmem) tma_prefetch_desc(&p.tmO);
       }
       __syncwarp();
       int nq[2] = {0, 0};
@@ -442,7 +453,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         if (elect_one()) {
           mma_qk<D, BF16>(tmem + t * C::kColS, qd, kd);
           umma_commit(bSfull(t));
-          if (last) umma_commit(bQfree(t, qbuf));
+          if (last && !C::kStoreOViaSmem) umma_commit(bQfree(t, qbuf));
         }
         __syncwarp();
       };
@@ -527,6 +538,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
     int ns = 0, nfin = 0;
     int npv = 0;  // P V of this tile issued so far (separate P: P_t is reused once the last one is done)
     bool ok = true;
+    // Q buffer whose O tile store may still be reading it; it is handed back
+    // to the producer after the next P handoff (or at the end), when the
+    // store has long finished reading.
+    int o_pending = -1;
+    auto release_staging = [&]() {
+      if (quad == 0 && lane == 0) {
+        tma_store_wait_read0();
+        mbar_arrive(bQfree(t, o_pending));  // the producer may load a later item's Q here
+      }
+      __syncwarp();
+      o_pending = -1;
+    };
     for (int mi = 0; mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
       const int item = item_of(mi);
       if (item >= p.n_items) continue;
@@ -626,15 +649,54 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         tc_fence_before();
         named_bar_arrive(kBarP + t, kBarHandoffThreads);  // P_t(j) (and O_t) written: P V of block j may go
         npv++;
+        if (C::kStoreOViaSmem && o_pending >= 0) release_staging();
       }
-      // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2
+      // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2.
+      // What does not need O (1/l, the LSE) is done while the last P V
+      // completes.
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const int grow = trow0 + row;
+      const bool live_row = grow < p.Nq;
+      if (ok && live_row && p.lse != nullptr)
+        p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
+            ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
+      const int qbuf = nfin % QB;  // this item's Q buffer (the MMA warp counts items the same way)
       ok = ok && mbar_wait_warp(bOfinal(t), nfin & 1, wc, kErrWaitOFinal);
       nfin++;
-      if (ok) {
+      if constexpr (C::kStoreOViaSmem) {
+        // Each thread writes its row into the Q buffer in the 128-byte
+        // swizzled layout of the O tensor map (16-byte chunk c of row r at
+        // chunk c ^ (r % 8): no bank conflicts); one TMA store then writes
+        // the tile, rows past Nq clipped by the map.  The buffer is free: the
+        // tile's last Q K^T completed before its S was seen.
+        const uint32_t stage = sQ + (t * QB + qbuf) * C::kQBytes;
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(ocol + cc * 32, r);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t chunk = static_cast<uint32_t>(cc * 4 + q) ^ static_cast<uint32_t>(row & 7);
+              st_shared_v4(stage + row * 128 + chunk * 16,
+                           pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv),
+                           pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv),
+                           pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv),
+                           pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv));
+            }
+          }
+          fence_proxy_async_smem();  // the rows are visible to the TMA store
+        }
+        named_bar_sync(kBarOStaged + t, 128);
+        if (ok && quad == 0 && lane == 0) {
+          tma_store_3d(&p.tmO, stage, 0, trow0, tbh);
+          tma_store_commit();
+        }
+        __syncwarp();
+        o_pending = qbuf;
+      } else if (ok) {
         tc_fence_after();
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        const int grow = trow0 + row;
-        const bool live_row = grow < p.Nq;
         uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
                         (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
 #pragma unroll
@@ -653,15 +715,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
             }
           }
         }
-        if (live_row && p.lse != nullptr)
-          p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
-              ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
       }
       // The next item's first P V (accumulate = 0) overwrites O_t; it is
       // issued only after the next P barrier, which these warps reach after
       // this read has completed (tcgen05.ld waits for its data).
       tc_fence_before();
     }
+    // the last O tile's global writes are complete before the CTA leaves
+    if (C::kStoreOViaSmem && o_pending >= 0) release_staging();
+    if (C::kStoreOViaSmem && quad == 0 && lane == 0) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();
