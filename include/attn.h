@@ -71,9 +71,11 @@ typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
 
 /* The kernels a call runs (see attn_fwd_ex). */
 typedef enum {
-  ATTN_PATH_PREFILL = 0,  /* tiled tcgen05 kernel: one launch */
-  ATTN_PATH_SPLIT_KV = 1, /* split-KV kernel + merge kernel: two launches */
-  ATTN_PATH_SHORT = 2     /* short-key kernel (Nk <= 128): one launch */
+  ATTN_PATH_PREFILL = 0,       /* tiled tcgen05 kernel: one launch */
+  ATTN_PATH_SPLIT_KV = 1,      /* split-KV kernel + merge kernel: two launches */
+  ATTN_PATH_SHORT = 2,         /* short-key kernel (Nk <= 128): one launch */
+  ATTN_PATH_PREFILL_SPLIT = 3  /* tiled tcgen05 kernel, work split evenly over the
+                                  SMs by K/V tiles (stream-K): one launch */
 } attn_path_t;
 
 /* Square attention, Nq = Nk = N.  Equivalent to attn_fwd_ex with Nq = Nk = N
@@ -86,38 +88,50 @@ attn_status_t attn_fwd(const void *Q, const void *K, const void *V, void *O, flo
  * decode step is Nq = 1 against an Nk-token cache).
  *
  * Paths: a call with Nk <= 128 runs the short-key kernel (every head's keys
- * fit one tile; the workspace, if any, is not used).  Otherwise, when a
- * workspace is given and the shape qualifies, the split-KV path runs; else
- * the tiled prefill kernel.  attn_fwd_path() says which.
+ * fit one tile; the workspace, if any, is not used).  Otherwise, with a
+ * workspace: the split-KV path for small query groups (decode); else, for a
+ * d = 128 call without a window whose 128-row tile pairs fill less than two
+ * waves of CTAs, the prefill kernel with its work split evenly over the SMs
+ * by K/V tiles.  Otherwise the tiled prefill kernel.  attn_fwd_path() says
+ * which.
  *
- * workspace/workspace_bytes: optional DEVICE scratch for the split-KV path
- * (cruxr.ai "FlashDecoding": the keys are split into chunks processed in
- * parallel, each yielding a partial max, sum and output, which a second step
- * combines by rescaling with exp(m_p - m)).  When workspace is NULL the
- * non-split path runs.  When it is given it must hold at least
+ * workspace/workspace_bytes: optional DEVICE scratch for the split paths.
+ * Both keep, for keys processed apart, a partial max, sum and output per
+ * query row and combine them by rescaling with exp(m_p - m) (cruxr.ai
+ * "FlashDecoding"): the split-KV path in a second kernel, the prefill split
+ * in the CTA that holds the first keys of the rows.  When workspace is NULL
+ * the non-split paths run.  When it is given it must hold at least
  * attn_fwd_workspace_bytes(...) bytes, 16-byte aligned, and must not be used
- * by another call that overlaps on the GPU. */
+ * by another call that overlaps on the GPU.  The prefill split has the CTAs
+ * of one launch wait (bounded) for each other, so it expects its CTAs (one
+ * per SM, at most the SM count) to be resident together; a concurrent
+ * kernel that holds SMs for longer than the wait limit ends the call with
+ * ATTN_ERR_TIMEOUT. */
 attn_status_t attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
                           int Hkv, int Nq, int Nk, int d, int causal, int window, float sm_scale,
                           attn_dtype_t dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Scratch bytes the split-KV path wants for this shape on the current device
- * (0 when the shape does not take that path: it serves GQA groups of at most
- * 32 query rows, i.e. (Hq / Hkv) * Nq <= 32, such as a decode step).  The
- * size depends on the device's SM count, which sets the number of chunks. */
+/* Scratch bytes the split paths want for this shape on the current device:
+ * the split-KV path's when the shape takes it (GQA groups of at most 32
+ * query rows, i.e. (Hq / Hkv) * Nq <= 32, such as a decode step), else the
+ * prefill split's when the shape takes it (d = 128, no window, fewer 128-row
+ * tile pairs than twice the SM count), else 0.  The size depends on the device's
+ * SM count. */
 size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 
 /* The path (attn_path_t) that attn_fwd_ex takes for these sizes on the
  * current device, with (with_workspace != 0) or without a workspace of
- * attn_fwd_workspace_bytes(...) bytes; -1 when the sizes are invalid.  Masks,
- * dtype and scale do not change the path.  No device work. */
+ * attn_fwd_workspace_bytes(...) bytes, for a call without a window; -1 when
+ * the sizes are invalid.  A window turns ATTN_PATH_PREFILL_SPLIT into
+ * ATTN_PATH_PREFILL; the causal flag, dtype and scale do not change the
+ * path.  No device work. */
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace);
 
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.
  * dev_buf must hold attn_fwd_host_staging_bytes(...) bytes (256-byte aligned);
- * that size includes the split-KV workspace when the shape takes that path.
+ * that size includes the workspace of a split path when the shape takes one.
  * The host buffers must stay valid until the stream reaches the end of the
  * call. */
 attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,

@@ -90,9 +90,21 @@ def test_workspace_errors_and_fallback(attn):
     with pytest.raises(attn.AttnError) as e:
         attn.flash_attn_forward(q, k, v, causal=True, workspace=small)
     assert e.value.status == attn.ATTN_ERR_INVALID_ARG
-    # more than 32 query rows per K/V head: no split, the workspace is unused
-    assert attn.attn_fwd_workspace_bytes(1, 32, 1, 2, 512, 128) == 0
-    assert attn.attn_fwd_workspace_bytes(1, 4, 4, 33, 512, 64) == 0
+    # more than 32 query rows per K/V head: no split-KV; a prefill this small
+    # takes the stream-K split instead, with its own size and the same check
+    assert attn.attn_fwd_path(1, 32, 1, 2, 512, 128, True) == attn.ATTN_PATH_PREFILL_SPLIT
+    need2 = attn.attn_fwd_workspace_bytes(1, 32, 1, 2, 512, 128)
+    assert need2 > need
+    shape2 = ai.AttnShape(1, 32, 1, 2, 512, 128, "bf16", True)
+    q2, k2, v2 = (t.cuda() for t in ai.make_qkv(shape2, config_id=63))
+    with pytest.raises(attn.AttnError) as e:
+        attn.flash_attn_forward(q2, k2, v2, causal=True, workspace=torch.empty(need2 - 4, dtype=torch.uint8,
+                                                                               device="cuda"))
+    assert e.value.status == attn.ATTN_ERR_INVALID_ARG
+    # a prefill with enough tile pairs for two waves takes no workspace, nor
+    # does one at d = 64
+    assert attn.attn_fwd_workspace_bytes(8, 12, 12, 2048, 2048, 128) == 0
+    assert attn.attn_fwd_workspace_bytes(1, 32, 1, 2, 512, 64) == 0
     assert attn.device_status() == attn.ATTN_OK
 
 
@@ -110,9 +122,14 @@ def test_workspace_reuse_is_stateless(attn, oracle_mod):
 
 @pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,ws,expect", [
     (4, 32, 8, 1, 8192, True, 1), (4, 32, 8, 1, 8192, False, 0), (4, 32, 8, 1, 128, True, 2),
-    (2, 4, 4, 64, 64, False, 2), (2, 4, 4, 256, 256, True, 0), (1, 32, 1, 2, 4096, True, 0),
-    (1, 4, 4, 33, 4096, True, 0), (2, 8, 0, 1, 64, False, -1)])
+    (2, 4, 4, 64, 64, False, 2), (2, 4, 4, 256, 256, True, 3), (2, 4, 4, 256, 256, False, 0),
+    (1, 32, 1, 2, 4096, True, 3), (1, 4, 4, 33, 4096, True, 3), (4, 32, 8, 8192, 8192, True, 0),
+    (8, 12, 12, 2048, 2048, True, 0), (2, 8, 0, 1, 64, False, -1)])
 def test_path_selection(attn, B, Hq, Hkv, Nq, Nk, ws, expect):
-    """attn_fwd_path: short keys first, then split-KV when a workspace is given
-    and the group has at most 32 query rows, else prefill; -1 on bad sizes."""
+    """attn_fwd_path (d = 128): short keys first; with a workspace, split-KV
+    when the group has at most 32 query rows, else the stream-K prefill split
+    when the tile pairs fill less than two waves of SMs; else prefill; -1 on
+    bad sizes.  At d = 64 the prefill split is never taken."""
     assert attn.attn_fwd_path(B, Hq, Hkv, Nq, Nk, 128, ws) == expect
+    if expect == 3:
+        assert attn.attn_fwd_path(B, Hq, Hkv, Nq, Nk, 64, ws) == 0

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "attn_decode.cuh"
@@ -118,9 +119,56 @@ static int device_sm_count() {
   return n;
 }
 
+// ---------------------------------------------------------------- stream-K split of the prefill
+// A d = 128 call whose items (tile pairs) fill less than two waves of CTAs
+// gets an even share of K/V tile steps per CTA instead of whole items, when
+// the caller passes a workspace and the call has no window (see FwdParams).
+static size_t round_up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static size_t split_ws_bytes(int d, int ctas) {
+  const size_t rows = static_cast<size_t>(ctas) * 2 * kBM;
+  return round_up256(rows * d * 4) + round_up256(rows * 8) + round_up256(static_cast<size_t>(ctas) * 2 * 4);
+}
+
+// Workspace bytes of the split (0: the shape does not take it), for a call
+// without a window on a device with `sms` SMs.  Only d = 128: an item cut
+// between CTAs costs its pieces a partial write, a flag and a merge on the
+// critical path (a few microseconds), which the better balance of the
+// heavier d = 128 tile steps repays and that of d = 64 does not.
+static size_t split_plan_bytes(const Shape &s, int sms) {
+  if (s.window > 0 || sms <= 0 || s.d != 128) return 0;
+  const long long zq = static_cast<long long>(s.B) * s.Hq;
+  const long long ntiles = (s.Nq + kBM - 1) / kBM;
+  const int group = s.Hq / s.Hkv;
+  const long long items = (group % 2 == 0) ? (zq / 2) * ntiles : zq * ((ntiles + 1) / 2);
+  if (items >= 2LL * sms) return 0;
+  return split_ws_bytes(s.d, std::min(sms, kMaxSplitCtas));
+}
+
+static std::atomic<unsigned> g_split_token{0};
+
+// One-time set-up of a prefill kernel on a device: its shared-memory size,
+// and whether it was built with the register count that the warpgroup
+// register split (setmaxnreg) is sized for: kThreads x kLaunchRegs
+// registers; any other allocation could stall.
+template <int D, bool BF16>
+static bool prefill_kernel_ready(int dev, bool split) {
+  static std::once_flag once[2][64];
+  static bool ok[2][64];
+  auto kern = split ? attn_fwd_kernel<D, BF16, true> : attn_fwd_kernel<D, BF16, false>;
+  const int k = split ? 1 : 0;
+  std::call_once(once[k][dev], [&] {
+    cudaFuncAttributes fa;
+    ok[k][dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      FwdCfg<D>::kSmemBytes) == cudaSuccess &&
+                 cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs == kLaunchRegs;
+  });
+  return ok[k][dev];
+}
+
 template <int D, bool BF16>
 static attn_status_t launch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
-                                   const Shape &s, cudaStream_t stream) {
+                                   const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -150,7 +198,14 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   // consecutive pairs (2r, 2r+1) otherwise.
   const int sms_now = device_sm_count();
   const long long ntiles = (s.Nq + kBM - 1) / kBM;
-  if (p.group % 2 == 0) {
+  const size_t split_bytes = ws ? split_plan_bytes(s, sms_now) : 0;
+  if (split_bytes > 0 && (ws_bytes < split_bytes || !aligned16(ws))) return ATTN_ERR_INVALID_ARG;
+  const bool split = split_bytes > 0;
+  if (split) {
+    // both tiles of every item busy: heads of a group, else row pairs
+    p.pair_mode = (p.group % 2 == 0) ? kPairHeads : kPairRows;
+    p.n_row_blocks = static_cast<int>(p.pair_mode == kPairHeads ? ntiles : (ntiles + 1) / 2);
+  } else if (p.group % 2 == 0) {
     p.pair_mode = kPairHeads;
     p.n_row_blocks = static_cast<int>(ntiles);
   } else if (zq * ntiles <= sms_now) {
@@ -171,37 +226,60 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.fd_slots = fastdiv_make(static_cast<uint32_t>(p.n_slots));
   p.fd_heads = fastdiv_make(static_cast<uint32_t>(p.pair_mode == kPairHeads ? s.Hq / 2 : s.Hq));
   p.fd_group = fastdiv_make(static_cast<uint32_t>(p.group));
+  int split_ctas = 0;
+  if (split) {
+    // Items in order, each its union range of K/V tile steps; CTA c starts
+    // at step c * W / G of the W steps in all.
+    long long total = 0;
+    std::vector<int> len(static_cast<size_t>(p.n_items));
+    for (int i = 0; i < p.n_items; ++i) {
+      const Item it = decode_item(p, i);
+      len[static_cast<size_t>(i)] = it.uend - it.ubeg;
+      total += len[static_cast<size_t>(i)];
+    }
+    split_ctas = static_cast<int>(std::min<long long>(std::min(sms_now, kMaxSplitCtas), total));
+    int item = 0;
+    long long before = 0;  // steps in items [0, item)
+    for (int c = 0; c < split_ctas; ++c) {
+      const long long target = total * c / split_ctas;
+      while (item < p.n_items && before + len[static_cast<size_t>(item)] <= target) {
+        before += len[static_cast<size_t>(item)];
+        ++item;
+      }
+      p.split_at[c] = make_int2(item, static_cast<int>(target - before));
+    }
+    p.split_at[split_ctas] = make_int2(p.n_items, 0);
+
+    unsigned tok = ++g_split_token;
+    if (tok == 0) tok = ++g_split_token;
+    p.token = tok;
+    const size_t rows = static_cast<size_t>(split_ctas) * 2 * kBM;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    p.ws_o = reinterpret_cast<float *>(base);
+    p.ws_ml = reinterpret_cast<float2 *>(base + round_up256(rows * D * 4));
+    p.ws_flag = reinterpret_cast<unsigned *>(base + round_up256(rows * D * 4) + round_up256(rows * 8));
+  }
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
 
-  auto kern = attn_fwd_kernel<D, BF16>;
+  auto kern = split ? attn_fwd_kernel<D, BF16, true> : attn_fwd_kernel<D, BF16, false>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  static std::once_flag attr_once[64];
-  static int n_sms[64];
-  static bool regs_ok[64];
-  std::call_once(attr_once[dev], [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    cudaDeviceGetAttribute(&n_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    // The warpgroup register split (setmaxnreg) is sized for a launch of
-    // kThreads x kLaunchRegs registers; any other allocation could stall.
-    cudaFuncAttributes fa;
-    regs_ok[dev] = cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs == kLaunchRegs;
-  });
-  if (!regs_ok[dev] || n_sms[dev] <= 0) return ATTN_ERR_UNSUPPORTED;
-  const int grid = static_cast<int>(std::min<long long>(items, n_sms[dev]));
+  if (!prefill_kernel_ready<D, BF16>(dev, split)) return ATTN_ERR_UNSUPPORTED;
+  const int grid = split ? split_ctas : static_cast<int>(std::min<long long>(items, sms_now));
+  if (grid <= 0) return ATTN_ERR_CUDA;
   if (launch_pdl(kern, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
-                                      const Shape &s, cudaStream_t stream) {
+                                      const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream) {
   const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
-  if (s.d == 64) return bf16 ? launch_prefill<64, true>(Q, K, V, O, LSE, s, stream)
-                             : launch_prefill<64, false>(Q, K, V, O, LSE, s, stream);
-  return bf16 ? launch_prefill<128, true>(Q, K, V, O, LSE, s, stream)
-              : launch_prefill<128, false>(Q, K, V, O, LSE, s, stream);
+  if (s.d == 64) return bf16 ? launch_prefill<64, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream)
+                             : launch_prefill<64, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream);
+  return bf16 ? launch_prefill<128, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream)
+              : launch_prefill<128, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- split-KV (decode) path
@@ -274,6 +352,7 @@ static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   return decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes;
 }
+
 
 template <int D, bool BF16>
 static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
@@ -425,6 +504,17 @@ static attn_status_t dispatch_short(const void *Q, const void *K, const void *V,
               : launch_short_t<128, false, 128>(Q, K, V, O, LSE, s, status, stream);
 }
 
+// Workspace of a call (no window): the split-KV decode plan's when the
+// shape has one (also for Nk <= 128, which the no-alloc entry runs through
+// it), else the stream-K split of the prefill, else none.
+static size_t workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  Shape s{B, Hq, Hkv, Nq, Nk, d, 0, 0, 1.f, ATTN_DTYPE_FP16};
+  const size_t dec = decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes;
+  if (dec > 0) return dec;
+  if (short_path(s)) return 0;
+  return split_plan_bytes(s, device_sm_count());
+}
+
 static attn_status_t run(const void *Q, const void *K, const void *V, void *O, float *LSE, const Shape &s,
                          void *ws, size_t ws_bytes, cudaStream_t stream) {
   attn_status_t st = validate(Q, K, V, O, LSE, s);
@@ -438,7 +528,7 @@ static attn_status_t run(const void *Q, const void *K, const void *V, void *O, f
       return dispatch_decode(Q, K, V, O, LSE, s, pl, static_cast<float *>(ws), stream);
     }
   }
-  return dispatch_prefill(Q, K, V, O, LSE, s, stream);
+  return dispatch_prefill(Q, K, V, O, LSE, s, ws, ws_bytes, stream);
 }
 
 }  // namespace attn
@@ -463,7 +553,7 @@ attn_status_t attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, 
 
 size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128) || Hq % Hkv) return 0;
-  return decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+  return workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
 }
 
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace) {
@@ -471,17 +561,16 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
   Shape s{B, Hq, Hkv, Nq, Nk, d, 0, 0, 1.f, ATTN_DTYPE_FP16};
   if (short_path(s)) return ATTN_PATH_SHORT;
   if (with_workspace && decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes > 0) return ATTN_PATH_SPLIT_KV;
+  if (with_workspace && split_plan_bytes(s, device_sm_count()) > 0) return ATTN_PATH_PREFILL_SPLIT;
   return ATTN_PATH_PREFILL;
 }
-
-static size_t round_up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_lse) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return 0;
   const size_t q = static_cast<size_t>(B) * Hq * Nq * d * 2;
   const size_t kv = static_cast<size_t>(B) * Hkv * Nk * d * 2;
   const size_t lse = with_lse ? static_cast<size_t>(B) * Hq * Nq * 4 : 0;
-  const size_t ws = decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+  const size_t ws = (d == 64 || d == 128) && Hq % Hkv == 0 ? workspace_bytes(B, Hq, Hkv, Nq, Nk, d) : 0;
   return round_up256(q) * 2 + round_up256(kv) * 2 + round_up256(lse) + round_up256(ws);
 }
 
@@ -503,7 +592,7 @@ attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *
   void *dO = base + round_up256(q) + 2 * round_up256(kv);
   float *dL = LSE_host ? reinterpret_cast<float *>(base + 2 * round_up256(q) + 2 * round_up256(kv)) : nullptr;
   const size_t lse_bytes = LSE_host ? static_cast<size_t>(B) * Hq * Nq * 4 : 0;
-  const size_t ws_bytes = decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+  const size_t ws_bytes = (d == 64 || d == 128) && Hq % Hkv == 0 ? workspace_bytes(B, Hq, Hkv, Nq, Nk, d) : 0;
   void *dW = ws_bytes ? base + 2 * round_up256(q) + 2 * round_up256(kv) + round_up256(lse_bytes) : nullptr;
   attn_status_t st = validate(dQ, dK, dV, dO, dL, s);
   if (st != ATTN_OK) return st;

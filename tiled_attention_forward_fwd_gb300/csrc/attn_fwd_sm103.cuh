@@ -48,7 +48,11 @@ enum DeviceError : int {
   kErrWaitS = 0x104,
   kErrWaitOFinal = 0x107,
   kErrWaitQFree = 0x108,
+  kErrWaitPartial = 0x109,
 };
+
+// Stream-K split of a call's work over at most this many CTAs.
+constexpr int kMaxSplitCtas = 256;
 
 struct FwdParams {
   CUtensorMap tmQ;  // (d, Nq, B*Hq)
@@ -69,6 +73,17 @@ struct FwdParams {
   FastDiv fd_group;  // / group
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
+  // Stream-K split (the kSplit kernel): the items, in order, form one
+  // sequence of K/V tile steps (each item its union range); CTA c takes the
+  // steps from split_at[c] to split_at[c + 1] (x = item, y = step within the
+  // item).  An item cut between CTAs is finished by the CTA holding its first
+  // steps: the others leave their partial O (fp32, not normalised) and (m, l)
+  // per row in the workspace and set their flag to `token`.
+  unsigned token;
+  float *ws_o;        // [CTA][tile][D][128 rows]: a warp's 32 rows of one column are contiguous
+  float2 *ws_ml;      // [CTA][tile][128 rows]
+  unsigned *ws_flag;  // [CTA][tile]
+  int2 split_at[kMaxSplitCtas + 1];
 };
 
 template <int D>
@@ -150,16 +165,22 @@ __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_
 }
 
 // One work item: up to two query tiles and the K/V tiles each one needs.
+// Under a stream-K split a CTA may hold only a piece of it: the K/V tiles
+// [ubeg, uend) of the item's union range [iubeg, iuend).
 struct Item {
   int b, kvh;
   int bh[2];    // b * Hq + h of each tile
   int row0[2];  // first query row of each tile
-  bool valid[2];
-  int beg[2], end[2];  // live K/V tile range of each tile
-  int ubeg, uend;      // union of the valid tiles' ranges
+  bool valid[2];       // the tile has K/V tiles in this piece
+  bool exists[2];      // the tile is part of the item
+  int beg[2], end[2];  // live K/V tile range of each tile in this piece
+  int ubeg, uend;      // union of the valid tiles' ranges in this piece
+  int obeg[2], oend[2];  // live K/V tile range of each tile in the whole item
+  int iubeg, iuend;      // union range of the whole item
+  int item;
 };
 
-__device__ __forceinline__ void tile_range(const FwdParams &p, int row0, int &beg, int &end) {
+ATTN_HD void tile_range(const FwdParams &p, int row0, int &beg, int &end) {
   const int i1 = min(row0 + kBM, p.Nq);
   const int off = p.Nk - p.Nq;
   const int p0 = row0 + off, p1 = i1 - 1 + off;
@@ -185,8 +206,9 @@ __device__ __forceinline__ void tile_range(const FwdParams &p, int row0, int &be
 //   kPairSingle  one row tile per item: when every tile can have its own SM
 enum PairMode : int { kPairRows = 0, kPairHeads = 1, kPairMirror = 2, kPairSingle = 3 };
 
-__device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
+ATTN_HD Item decode_item(const FwdParams &p, int item) {
   Item it;
+  it.item = item;
   int idx, slot, hs;
   fastdiv_divmod(p.fd_slots, item, idx, slot);  // idx: longest items first
   fastdiv_divmod(p.fd_heads, slot, it.b, hs);
@@ -219,14 +241,70 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int item) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     it.valid[t] = it.row0[t] < p.Nq;
+    it.exists[t] = it.valid[t];
     it.beg[t] = it.end[t] = 0;
     if (it.valid[t]) {
       tile_range(p, it.row0[t], it.beg[t], it.end[t]);
-      it.ubeg = min(it.ubeg, it.beg[t]);
-      it.uend = max(it.uend, it.end[t]);
+      it.ubeg = it.ubeg < it.beg[t] ? it.ubeg : it.beg[t];
+      it.uend = it.uend > it.end[t] ? it.uend : it.end[t];
     }
+    it.obeg[t] = it.beg[t];
+    it.oend[t] = it.end[t];
   }
+  it.iubeg = it.ubeg;
+  it.iuend = it.uend;
   return it;
+}
+
+// Restrict an item to the K/V tiles [iubeg + s0, iubeg + s1) of its union
+// range; a tile with none of them is not valid in the piece.
+ATTN_HD void clip_item(Item &it, int s0, int s1) {
+  const int lo = it.iubeg + s0;
+  const int hi = (it.iubeg + s1 < it.iuend) ? it.iubeg + s1 : it.iuend;
+  it.ubeg = lo;
+  it.uend = hi;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    it.beg[t] = it.obeg[t] > lo ? it.obeg[t] : lo;
+    it.end[t] = it.oend[t] < hi ? it.oend[t] : hi;
+    it.valid[t] = it.exists[t] && it.beg[t] < it.end[t];
+  }
+}
+
+// Items are handed to the persistent CTAs in passes of gridDim.x, alternating
+// direction ("snake"): with items sorted longest first, every CTA gets a
+// similar total.  Returns the m-th item of this CTA (>= n_items: none).
+__device__ __forceinline__ int item_of(int m) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return m * g + ((m & 1) ? (g - 1 - c) : c);
+}
+
+// Number of work pieces of this CTA: passes over the item list, or the
+// items that its stream-K range touches.
+template <bool kSplit>
+__device__ __forceinline__ int num_pieces(const FwdParams &p) {
+  if constexpr (!kSplit) return (p.n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  const int2 s = p.split_at[blockIdx.x], e = p.split_at[blockIdx.x + 1];
+  const int last = (e.y > 0) ? e.x : e.x - 1;  // last item touched
+  if (s.x > last || (s.x == e.x && s.y >= e.y)) return 0;
+  return last - s.x + 1;
+}
+
+// The k-th piece of this CTA's work; false when there is none (the last pass
+// over the item list may be short).
+template <bool kSplit>
+__device__ __forceinline__ bool piece_at(const FwdParams &p, int k, Item &it) {
+  if constexpr (!kSplit) {
+    const int item = item_of(k);
+    if (item >= p.n_items) return false;
+    it = decode_item(p, item);
+    return true;
+  }
+  const int2 s = p.split_at[blockIdx.x], e = p.split_at[blockIdx.x + 1];
+  const int item = s.x + k;
+  it = decode_item(p, item);
+  clip_item(it, k == 0 ? s.y : 0, item == e.x ? e.y : (1 << 30));
+  return true;
 }
 
 // Row max of a 128-column S row: eight independent chains, columns 0-15 by
@@ -275,15 +353,10 @@ constexpr uint32_t kBarP = 1, kBarSRead = 3, kBarHandoffThreads = 128 + 32;
 // Named barrier of one softmax warpgroup alone: its O tile is staged.
 constexpr uint32_t kBarOStaged = 5;
 
-// Items are handed to the persistent CTAs in passes of gridDim.x, alternating
-// direction ("snake"): with items sorted longest first, every CTA gets a
-// similar total.  Returns the m-th item of this CTA (>= n_items: none).
-__device__ __forceinline__ int item_of(int m) {
-  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  return m * g + ((m & 1) ? (g - 1 - c) : c);
-}
 
-template <int D, bool BF16>
+// kSplit: the stream-K schedule (FwdParams::split_at); the plain schedule
+// otherwise, compiled without any of the split's code.
+template <int D, bool BF16, bool kSplit>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int NS = C::kStages;
@@ -331,6 +404,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
     }
     fence_mbar_init();
   }
+  if (warp == 0 && elect_one()) {
+    // the tensor maps are launch parameters: fetch them while the previous
+    // kernel on the stream may still run
+    tma_prefetch_desc(&p.tmQ);
+    tma_prefetch_desc(&p.tmK);
+    tma_prefetch_desc(&p.tmV);
+    if (C::kStoreOViaSmem) tma_prefetch_desc(&p.tmO);
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
@@ -348,20 +429,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       // ============================================================ TMA producer
       // The loop runs on the whole warp (uniform control flow and addresses);
       // one elected lane issues each copy.
-      if (elect_one()) {
-        tma_prefetch_desc(&p.tmQ);
-        tma_prefetch_desc(&p.tmK);
-        tma_prefetch_desc(&p.tmV);
-        if (C::kStoreOViaSmem) tma_prefetch_desc(&p.tmO);
-      }
-      __syncwarp();
       int nq[2] = {0, 0};
       int ckv = 0;
       bool ok = true;
-      for (int mi = 0; ok && mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
-        const int item = item_of(mi);
-        if (item >= p.n_items) continue;
-        const Item it = decode_item(p, item);
+      const int npieces = num_pieces<kSplit>(p);
+      for (int pk = 0; ok && pk < npieces; ++pk) {
+        Item it;
+        if (!piece_at<kSplit>(p, pk, it)) continue;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || !it.valid[t]) continue;
@@ -473,10 +547,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         }
         pending = false;
       };
-      for (int mi = 0; mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
-        const int item = item_of(mi);
-        if (item >= p.n_items) continue;
-        const Item it = decode_item(p, item);
+      const int npieces = num_pieces<kSplit>(p);
+      for (int pk = 0; pk < npieces; ++pk) {
+        Item it;
+        if (!piece_at<kSplit>(p, pk, it)) continue;
         const bool tvalid = t ? it.valid[1] : it.valid[0];
         const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
         const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
@@ -550,10 +624,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       __syncwarp();
       o_pending = -1;
     };
-    for (int mi = 0; mi * static_cast<int>(gridDim.x) < p.n_items; ++mi) {
-      const int item = item_of(mi);
-      if (item >= p.n_items) continue;
-      const Item it = decode_item(p, item);
+    const int npieces = num_pieces<kSplit>(p);
+    for (int pk = 0; pk < npieces; ++pk) {
+      Item it;
+      if (!piece_at<kSplit>(p, pk, it)) continue;
       // this warpgroup's tile, as scalars (t is not a compile-time index)
       const bool tvalid = t ? it.valid[1] : it.valid[0];
       if (!tvalid) continue;
@@ -651,19 +725,98 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         npv++;
         if (C::kStoreOViaSmem && o_pending >= 0) release_staging();
       }
-      // ---- epilogue of this tile: O / l -> 16-bit, LSE = (m + log2 l) ln 2.
-      // What does not need O (1/l, the LSE) is done while the last P V
+      // ---- epilogue of this tile.  A whole item: O / l -> 16-bit and
+      // LSE = (m + log2 l) ln 2.  Under a stream-K split, a piece after the
+      // item's first steps hands its partial (O, m, l) on through the
+      // workspace; the item's first piece merges the others' partials into its
+      // own before O / l.  What does not need O is done while the last P V
       // completes.
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      // (the piece is decoded again here, so that its ranges need no
+      // registers during the K/V loop)
+      Item ie{};
+      bool part_out = false, merge_in = false;
+      if constexpr (kSplit) {
+        piece_at<kSplit>(p, pk, ie);
+        part_out = ie.ubeg > ie.iubeg;
+        merge_in = ie.ubeg == ie.iubeg && ie.uend < ie.iuend;
+      }
       const int grow = trow0 + row;
       const bool live_row = grow < p.Nq;
-      if (ok && live_row && p.lse != nullptr)
+      const int tobeg = t ? ie.obeg[1] : ie.obeg[0];
+      const int toend = t ? ie.oend[1] : ie.oend[0];
+      // The pieces after this one of the item are the first pieces of the
+      // next CTAs; the tile has a partial in those whose steps it reaches.
+      auto part_live = [&](int c) {
+        const int2 a = p.split_at[c], b = p.split_at[c + 1];
+        const int lo = ie.iubeg + a.y, hi = (b.x == ie.item) ? ie.iubeg + b.y : ie.iuend;
+        return max(tobeg, lo) < min(toend, hi);
+      };
+      auto part_ml = [&](int c) {
+        return __ldcg(p.ws_ml + (static_cast<size_t>(c) * 2 + t) * kBM + row);
+      };
+      float mf = m, lf = l;  // merged running max and sum
+      if (merge_in) {
+        for (int c = blockIdx.x + 1; c < static_cast<int>(gridDim.x) && p.split_at[c].x == ie.item; ++c) {
+          if (!part_live(c)) continue;
+          ok = ok && flag_wait(p.ws_flag + c * 2 + t, p.token, wc, kErrWaitPartial);
+          if (!ok) break;
+          const float2 ml = part_ml(c);
+          if (ml.y > 0.f) {
+            const float mn = fmaxf(mf, ml.x);
+            lf = (mf == -INFINITY ? 0.f : lf * ex2_approx(mf - mn)) + ml.y * ex2_approx(ml.x - mn);
+            mf = mn;
+          }
+        }
+      }
+      const float a_own = (m == -INFINITY) ? 0.f : ex2_approx(m - mf);  // 1 unless merged
+      const float inv = part_out ? 1.f : ((lf > 0.f) ? 1.f / lf : 0.f);
+      if (ok && live_row && p.lse != nullptr && !part_out)
         p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
-            ((l > 0.f) ? m + log2f(l) : -INFINITY) * 0.69314718055994530942f;
+            ((lf > 0.f) ? mf + log2f(lf) : -INFINITY) * 0.69314718055994530942f;
       const int qbuf = nfin % QB;  // this item's Q buffer (the MMA warp counts items the same way)
       ok = ok && mbar_wait_warp(bOfinal(t), nfin & 1, wc, kErrWaitOFinal);
       nfin++;
-      if constexpr (C::kStoreOViaSmem) {
+      // 32 columns of this row's output before the 1/l: O_t from TMEM, plus
+      // the other pieces' partials when merging
+      auto out_chunk = [&](int cc, float (&v)[32]) {
+        uint32_t r[32];
+        tmem_ld32(ocol + cc * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if (merge_in) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= a_own;
+          for (int c = blockIdx.x + 1; c < static_cast<int>(gridDim.x) && p.split_at[c].x == ie.item; ++c) {
+            if (!part_live(c)) continue;
+            const float2 ml = part_ml(c);
+            if (!(ml.y > 0.f)) continue;
+            const float sp = ex2_approx(ml.x - mf);
+            const float *src = p.ws_o + ((static_cast<size_t>(c) * 2 + t) * D + cc * 32) * kBM + row;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = fmaf(__ldcg(src + i * kBM), sp, v[i]);
+          }
+        }
+      };
+      if (part_out) {
+        // partial O (not normalised) and (m, l) of each row, then the flag:
+        // the barrier orders every thread's writes before the one release
+        if (ok) {
+          tc_fence_after();
+          float *dst = p.ws_o + (static_cast<size_t>(blockIdx.x) * 2 + t) * D * kBM + row;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float v[32];
+            out_chunk(cc, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) __stcg(dst + (cc * 32 + i) * kBM, v[i]);
+          }
+          __stcg(p.ws_ml + (static_cast<size_t>(blockIdx.x) * 2 + t) * kBM + row, make_float2(m, l));
+        }
+        named_bar_sync(kBarOStaged + t, 128);
+        if (ok && quad == 0 && lane == 0) st_release_gpu(p.ws_flag + blockIdx.x * 2 + t, p.token);
+        __syncwarp();
+        if constexpr (C::kStoreOViaSmem) o_pending = qbuf;  // no store read the Q buffer
+      } else if constexpr (C::kStoreOViaSmem) {
         // Each thread writes its row into the Q buffer in the 128-byte
         // swizzled layout of the O tensor map (16-byte chunk c of row r at
         // chunk c ^ (r % 8): no bank conflicts); one TMA store then writes
@@ -674,16 +827,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(ocol + cc * 32, r);
+            float v[32];
+            out_chunk(cc, v);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t chunk = static_cast<uint32_t>(cc * 4 + q) ^ static_cast<uint32_t>(row & 7);
-              st_shared_v4(stage + row * 128 + chunk * 16,
-                           pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv),
-                           pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv),
-                           pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv),
-                           pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv));
+              st_shared_v4(stage + row * 128 + chunk * 16, pack2<BF16>(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv),
+                           pack2<BF16>(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv),
+                           pack2<BF16>(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv),
+                           pack2<BF16>(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv));
             }
           }
           fence_proxy_async_smem();  // the rows are visible to the TMA store
@@ -701,16 +853,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
                         (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(ocol + cc * 32, r);
+          float v[32];
+          out_chunk(cc, v);
           if (live_row) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 w;
-              w.x = pack2<BF16>(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv);
-              w.y = pack2<BF16>(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv);
-              w.z = pack2<BF16>(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
-              w.w = pack2<BF16>(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
+              w.x = pack2<BF16>(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv);
+              w.y = pack2<BF16>(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv);
+              w.z = pack2<BF16>(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv);
+              w.w = pack2<BF16>(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv);
               *reinterpret_cast<uint4 *>(orow + cc * 64 + q * 16) = w;
             }
           }
@@ -721,9 +873,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       // this read has completed (tcgen05.ld waits for its data).
       tc_fence_before();
     }
-    // the last O tile's global writes are complete before the CTA leaves
+    // the last O tile store has read its staging buffer before the CTA
+    // leaves (its global writes complete with the grid)
     if (C::kStoreOViaSmem && o_pending >= 0) release_staging();
-    if (C::kStoreOViaSmem && quad == 0 && lane == 0) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();

@@ -125,6 +125,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Flags in global memory shared between CTAs of one grid.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait of the calling thread for *flag == value (set by another CTA
+// of the same grid).  Returns false on timeout or when the CTA has aborted.
+__device__ __forceinline__ bool flag_wait(const unsigned *flag, unsigned value, const WaitCtl &w, int code) {
+  if (ld_acquire_gpu(flag) == value) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_gpu(flag) == value) return true;
+    if ((it & 31u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        *w.abort_flag = 1;
+        atomicCAS(w.status, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-collective bounded wait: every lane polls in step and every decision
 // is taken warp-wide, so the warp never diverges and stays converged for the
 // .sync.aligned tcgen05 instructions that follow.
