@@ -325,10 +325,11 @@ __device__ __forceinline__ float softmax_max8(const float (&mx)[8]) {
 
 // p = 2^(s * sm_scale * log2 e - m) for the 128 columns of a row, two per
 // packed FMA, written to TMEM as packed 16-bit pairs (32 columns per chunk);
-// rs gets the fp32 sum.
-template <bool BF16>
+// rs gets the fp32 sum.  before_store() runs once, after the first chunk's
+// exp2 and before its store: a wait for P to be free costs no exp2 latency.
+template <bool BF16, typename BeforeStore>
 __device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x2, float m, float2 (&rs)[2],
-                                          uint32_t pcol) {
+                                          uint32_t pcol, BeforeStore before_store) {
   const float mref = (m == -INFINITY) ? 0.f : m;
   const float2 negm = make_float2(-mref, -mref);
   rs[0] = rs[1] = make_float2(0.f, 0.f);
@@ -343,6 +344,7 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x
       pk[i] = pack2<BF16>(e.x, e.y);
       rs[i & 1] = fadd2(rs[i & 1], e);
     }
+    if (cc == 0) before_store();
     tmem_st16(pcol + cc * 16, pk);
   }
 }
@@ -663,12 +665,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
               if (!key_live(key0 + cc, pos, p.Nk, p.causal, p.window)) sr[cc] = 0xff800000u;  // -inf
           }
           const bool first = (j == tbeg);
-          if constexpr (C::kSeparateP) {
-            // P_t and O_t are free once the P V of block j-1 has completed
-            // (at an item's first block the previous O-final wait covered it).
-            if (!first) ok = mbar_wait_warp(bPVdone(t), (npv - 1) & 1, wc, kErrWaitS);
-            tc_fence_after();
-          }
+          // Separate P: P_t and O_t are free once the P V of block j-1 has
+          // completed (at an item's first block the previous O-final wait
+          // covered it).  The wait comes before the first P store; every
+          // later access to P_t or O_t (a redo pass, the O rescale) follows.
+          bool pv_waited = first;
+          auto before_store = [&]() {
+            if constexpr (C::kSeparateP) {
+              if (!pv_waited) {
+                ok = mbar_wait_warp(bPVdone(t), (npv - 1) & 1, wc, kErrWaitS) && ok;
+                pv_waited = true;
+              }
+              tc_fence_after();
+            }
+          };
           const float2 sl2x2 = make_float2(sl2, sl2);
           float2 rs[2];
           float mx[8];
@@ -684,7 +694,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
               alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
               m = m_new;
             }
-            softmax_p<BF16>(sr, sl2x2, m, rs, pcol);
+            softmax_p<BF16>(sr, sl2x2, m, rs, pcol, before_store);
           } else {
             // Speculative pass with the current reference max, no row max.
             // No p exceeds the row sum, so a sum of at most 2^8 shows that
@@ -692,7 +702,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
             // (lazy rescale).  Otherwise, or while the row has no finite max
             // yet, the row max is taken and the pass redone; after an item's
             // first blocks that is rare.
-            softmax_p<BF16>(sr, sl2x2, m, rs, pcol);
+            softmax_p<BF16>(sr, sl2x2, m, rs, pcol, before_store);
             const float rsum = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
             rescale = __any_sync(0xffffffffu, !(rsum <= kRescaleSum) || m == -INFINITY);
             if (rescale) {
@@ -700,7 +710,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
               const float m_new = fmaxf(m, softmax_max8(mx) * sl2);
               alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
               m = m_new;
-              softmax_p<BF16>(sr, sl2x2, m, rs, pcol);
+              softmax_p<BF16>(sr, sl2x2, m, rs, pcol, before_store);
             }
           }
           l = l * alpha + ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
