@@ -197,11 +197,12 @@ def prepare(workload: str, device):
         path = attn.attn_fwd_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d, wsb > 0)
         if path == attn.ATTN_PATH_PREFILL_SPLIT and shape.window > 0:
             path = attn.ATTN_PATH_PREFILL  # the split is not used with a window
-        split = path in (attn.ATTN_PATH_SPLIT_KV, attn.ATTN_PATH_PREFILL_SPLIT)
+        split = path in (attn.ATTN_PATH_SPLIT_KV, attn.ATTN_PATH_SPLIT_KV_FUSED, attn.ATTN_PATH_PREFILL_SPLIT)
         c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device) if split else None
         c["path"] = path
         c["kernel"] = {attn.ATTN_PATH_PREFILL: "attn_fwd_kernel", attn.ATTN_PATH_PREFILL_SPLIT: "attn_fwd_kernel",
-                       attn.ATTN_PATH_SPLIT_KV: "attn_decode_kernel", attn.ATTN_PATH_SHORT: "attn_short_kernel"}[path]
+                       attn.ATTN_PATH_SPLIT_KV: "attn_decode_kernel", attn.ATTN_PATH_SPLIT_KV_FUSED: "attn_decode_kernel",
+                       attn.ATTN_PATH_SHORT: "attn_short_kernel"}[path]
         c["launches"] = 2 if path == attn.ATTN_PATH_SPLIT_KV else 1  # split kernel + merge kernel
         calls.append(c)
     return calls

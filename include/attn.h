@@ -74,8 +74,10 @@ typedef enum {
   ATTN_PATH_PREFILL = 0,       /* tiled tcgen05 kernel: one launch */
   ATTN_PATH_SPLIT_KV = 1,      /* split-KV kernel + merge kernel: two launches */
   ATTN_PATH_SHORT = 2,         /* short-key kernel (Nk <= 128): one launch */
-  ATTN_PATH_PREFILL_SPLIT = 3  /* tiled tcgen05 kernel, work split evenly over the
+  ATTN_PATH_PREFILL_SPLIT = 3, /* tiled tcgen05 kernel, work split evenly over the
                                   SMs by K/V tiles (stream-K): one launch */
+  ATTN_PATH_SPLIT_KV_FUSED = 4 /* split-KV kernel whose last chunk of each query
+                                  group merges the group (small merges): one launch */
 } attn_path_t;
 
 /* Square attention, Nq = Nk = N.  Equivalent to attn_fwd_ex with Nq = Nk = N

@@ -27,7 +27,7 @@ def run_split(attn, shape, q, k, v):
     nbytes = attn.attn_fwd_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d)
     assert nbytes > 0, "shape should qualify for the split-KV path"
     path = attn.attn_fwd_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d, True)
-    if path == attn.ATTN_PATH_SPLIT_KV:
+    if path in (attn.ATTN_PATH_SPLIT_KV, attn.ATTN_PATH_SPLIT_KV_FUSED):
         ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         return pu.run_cuda(shape, q, k, v, workspace=ws)
     assert path == attn.ATTN_PATH_SHORT and shape.Nk <= 128
@@ -121,13 +121,15 @@ def test_workspace_reuse_is_stateless(attn, oracle_mod):
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,ws,expect", [
-    (4, 32, 8, 1, 8192, True, 1), (4, 32, 8, 1, 8192, False, 0), (4, 32, 8, 1, 128, True, 2),
+    (4, 32, 8, 1, 8192, True, 4), (4, 32, 1, 1, 8192, True, 1), (4, 32, 8, 1, 8192, False, 0),
+    (4, 32, 8, 1, 128, True, 2),
     (2, 4, 4, 64, 64, False, 2), (2, 4, 4, 256, 256, True, 3), (2, 4, 4, 256, 256, False, 0),
     (1, 32, 1, 2, 4096, True, 3), (1, 4, 4, 33, 4096, True, 3), (4, 32, 8, 8192, 8192, True, 0),
     (8, 12, 12, 2048, 2048, True, 0), (2, 8, 0, 1, 64, False, -1)])
 def test_path_selection(attn, B, Hq, Hkv, Nq, Nk, ws, expect):
     """attn_fwd_path (d = 128): short keys first; with a workspace, split-KV
-    when the group has at most 32 query rows, else the stream-K prefill split
+    when the group has at most 32 query rows (its merge fused into the split
+    kernel when small: 4 query rows x 9 chunks), else the stream-K prefill split
     when the tile pairs fill less than two waves of SMs; else prefill; -1 on
     bad sizes.  At d = 64 the prefill split is never taken."""
     assert attn.attn_fwd_path(B, Hq, Hkv, Nq, Nk, 128, ws) == expect

@@ -56,7 +56,7 @@ def _chain(attn, graph: bool):
 
     assert attn.attn_fwd_path(2, 4, 4, 2048, 2048, 64, False) == attn.ATTN_PATH_PREFILL
     assert attn.attn_fwd_path(2, 4, 2, 2048, 64, 64, False) == attn.ATTN_PATH_SHORT
-    assert attn.attn_fwd_path(2, 4, 1, 1, 3000, 64, True) == attn.ATTN_PATH_SPLIT_KV
+    assert attn.attn_fwd_path(2, 4, 1, 1, 3000, 64, True) in (attn.ATTN_PATH_SPLIT_KV, attn.ATTN_PATH_SPLIT_KV_FUSED)
     if graph:
         run()  # warm the launch path before capture
         torch.cuda.synchronize()

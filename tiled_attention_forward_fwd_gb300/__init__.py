@@ -29,6 +29,7 @@ ATTN_PATH_PREFILL = 0
 ATTN_PATH_SPLIT_KV = 1
 ATTN_PATH_SHORT = 2
 ATTN_PATH_PREFILL_SPLIT = 3
+ATTN_PATH_SPLIT_KV_FUSED = 4
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",

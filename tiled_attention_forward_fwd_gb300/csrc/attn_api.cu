@@ -285,7 +285,9 @@ static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *
 // ---------------------------------------------------------------- split-KV (decode) path
 struct DecPlan {
   int nchunks = 0, chunk_keys = 0;
-  size_t bytes = 0;  // 0: this shape does not take the split-KV path
+  bool fused = false;    // the split kernel merges the chunks itself
+  size_t flag_off = 0;   // byte offset of the per-(group, chunk) flags
+  size_t bytes = 0;      // 0: this shape does not take the split-KV path
 };
 
 
@@ -345,7 +347,13 @@ static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   chunk_keys = ((chunk_keys + kDecKeys - 1) / kDecKeys) * kDecKeys;
   pl.nchunks = (Nk + chunk_keys - 1) / chunk_keys;
   pl.chunk_keys = chunk_keys;
-  pl.bytes = static_cast<size_t>(B) * Hq * Nq * pl.nchunks * (d + 1) * sizeof(float);
+  // A small merge (rows x chunks x d of a group) is done by the split
+  // kernel's CTA of each group's last chunk; a large one by the merge kernel,
+  // one CTA per row.
+  pl.fused = R * pl.nchunks * d <= kDecFusedMerge;
+  const size_t part = static_cast<size_t>(B) * Hq * Nq * pl.nchunks * (d + 1) * sizeof(float);
+  pl.flag_off = (part + 15) & ~size_t(15);
+  pl.bytes = pl.flag_off + static_cast<size_t>(units) * pl.nchunks * sizeof(unsigned);
   return pl;
 }
 
@@ -384,6 +392,15 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   p.kv_hi = s.Nk;
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
+  if (pl.fused) {
+    p.fused = 1;
+    unsigned tok = ++g_split_token;
+    if (tok == 0) tok = ++g_split_token;
+    p.token = tok;
+    p.flags = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(ws) + pl.flag_off);
+    p.O = O;
+    p.lse = LSE;
+  }
   // (the plan already set the shared-memory attribute of both kernels)
   if (decode_ctas_per_sm(D, p.R <= 16 ? 1 : 2) <= 0) return ATTN_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(zk));
@@ -391,6 +408,7 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
       (p.R <= 16) ? launch_pdl(attn_decode_kernel<D, BF16, 1>, grid, dim3(kDecThreads), DecCfg<D, 1>::kSmemBytes, stream, p)
                   : launch_pdl(attn_decode_kernel<D, BF16, 2>, grid, dim3(kDecThreads), DecCfg<D, 2>::kSmemBytes, stream, p);
   if (le != cudaSuccess || cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (pl.fused) return ATTN_OK;
   // The merge kernel is a programmatic dependent: it may launch while the
   // split kernel runs and waits (griddepcontrol.wait) for its results.
   const int rows = s.B * s.Hq * s.Nq;
@@ -560,7 +578,8 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return -1;
   Shape s{B, Hq, Hkv, Nq, Nk, d, 0, 0, 1.f, ATTN_DTYPE_FP16};
   if (short_path(s)) return ATTN_PATH_SHORT;
-  if (with_workspace && decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes > 0) return ATTN_PATH_SPLIT_KV;
+  const DecPlan dp = decode_plan(B, Hq, Hkv, Nq, Nk, d);
+  if (with_workspace && dp.bytes > 0) return dp.fused ? ATTN_PATH_SPLIT_KV_FUSED : ATTN_PATH_SPLIT_KV;
   if (with_workspace && split_plan_bytes(s, device_sm_count()) > 0) return ATTN_PATH_PREFILL_SPLIT;
   return ATTN_PATH_PREFILL;
 }

@@ -21,9 +21,13 @@
 // ldmatrix (transposed for V), and O is rescaled only when a row's max grew
 // by more than 2^8.  At the end the 4 warps are merged in shared memory and
 // the chunk's normalised O and its log2-domain log-sum-exp go to the
-// caller's workspace.  Kernel 2, launched as a programmatic dependent so that
-// its launch overlaps kernel 1, merges the chunks of every row (one CTA per
-// row) and writes O (16-bit) and LSE.
+// caller's workspace.  When the merge is small (rows x chunks x d of a group
+// at most kDecFusedMerge floats), the CTA of a group's last chunk merges the
+// group's chunks itself once every chunk has published its partial (a flag
+// set to the launch's token with release semantics).  Otherwise kernel 2,
+// launched as a programmatic dependent so that its launch overlaps kernel 1,
+// merges the chunks of every row (one CTA per row) and writes O (16-bit) and
+// LSE.
 #pragma once
 
 #include <stddef.h>
@@ -37,8 +41,9 @@ constexpr int kDecWarps = 4;     // consumer warps: each owns 16 keys of every t
 constexpr int kDecThreads = 32 * kDecWarps + 32;  // + one TMA producer warp
 constexpr int kDecMaxRows = 32;  // query rows of one group handled by one CTA
 constexpr int kDecMaxChunks = 1024;  // key chunks per group (bounds the merge kernel's shared memory)
+constexpr int kDecFusedMerge = 8192;  // rows x chunks x d of a group merged by the split kernel itself
 
-enum DecodeError : int { kErrDecWaitKV = 0x201 };
+enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecWaitPartial = 0x202 };
 
 struct DecParams {
   CUtensorMap tmK;  // (d, Nk, B*Hkv), box 64 x 64 x 1, 128B swizzle
@@ -46,6 +51,13 @@ struct DecParams {
   const void *Q;    // (B, Hq, Nq, d), 16-bit
   float *ws;        // [B*Hq*Nq][nchunks][d]: normalised O of each chunk
   float *ws_lse;    // [B*Hq*Nq][nchunks]: log2 LSE of each chunk (-inf: no live key)
+  // fused merge (fused != 0): flags [B*Hkv][nchunks] set to `token` once a
+  // chunk's partial is written; O and LSE written by the last chunk's CTA
+  int fused;
+  unsigned token;
+  unsigned *flags;
+  void *O;
+  float *lse;
   int *status;
   int B, Hq, Hkv, Nq, Nk, group, R;  // R = group * Nq query rows per CTA
   int causal, window;
@@ -421,6 +433,60 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
     const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
     *reinterpret_cast<float4 *>(p.ws + (grow * p.nchunks + chunk) * D + c) =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  if (!p.fused) return;
+  // ---- fused merge: publish this chunk; the group's last chunk merges
+  __syncthreads();  // every thread's partial is written before the one release
+  unsigned *fl = p.flags + static_cast<size_t>(bk) * p.nchunks;
+  if (threadIdx.x == 0) st_release_gpu(fl + chunk, p.token);
+  if (chunk != p.nchunks - 1) return;
+  // The other chunks of the group have lower block indices: they were
+  // launched before this CTA and wait for nothing of it.
+  bool got = true;
+  for (int c = threadIdx.x; c < p.nchunks - 1; c += kDecThreads)
+    got = got && flag_wait(fl + c, p.token, wc, kErrDecWaitPartial);
+  if (__syncthreads_or(!got)) return;
+  // per row: the chunk weights 2^(lse_c - M) and 1 / their sum (shared
+  // memory: the ring is idle)
+  float *linv = oacc;               // [R]
+  float *wts = oacc + kDecMaxRows;  // [R][nchunks]
+  if (threadIdx.x < p.R) {
+    const int r = threadIdx.x;
+    const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
+    const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
+    const float *lr = p.ws_lse + grow * p.nchunks;
+    float M = -INFINITY;
+    for (int c = 0; c < p.nchunks; ++c) M = fmaxf(M, __ldcg(lr + c));
+    float L = 0.f;
+    for (int c = 0; c < p.nchunks; ++c) {
+      const float lc = __ldcg(lr + c);
+      const float w = (lc == -INFINITY) ? 0.f : ex2_approx(lc - M);
+      wts[r * p.nchunks + c] = w;
+      L += w;
+    }
+    linv[r] = (L > 0.f) ? 1.f / L : 0.f;
+    if (p.lse != nullptr) p.lse[grow] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < p.R * (D / 4); idx += kDecThreads) {
+    const int r = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+    const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
+    const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
+    const float4 *src = reinterpret_cast<const float4 *>(p.ws + grow * p.nchunks * D + c4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < p.nchunks; ++c) {
+      const float w = wts[r * p.nchunks + c];
+      const float4 v = __ldcg(src + static_cast<size_t>(c) * (D / 4));
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    const float inv = linv[r];
+    uint2 out;
+    out.x = pack2<BF16>(acc.x * inv, acc.y * inv);
+    out.y = pack2<BF16>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.O) + grow * D + c4) = out;
   }
 }
 
