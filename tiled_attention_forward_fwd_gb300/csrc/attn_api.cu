@@ -152,11 +152,18 @@ static std::atomic<unsigned> g_split_token{0};
 // register split (setmaxnreg) is sized for: kThreads x kLaunchRegs
 // registers; any other allocation could stall.
 template <int D, bool BF16>
-static bool prefill_kernel_ready(int dev, bool split) {
-  static std::once_flag once[2][64];
-  static bool ok[2][64];
-  auto kern = split ? attn_fwd_kernel<D, BF16, true> : attn_fwd_kernel<D, BF16, false>;
-  const int k = split ? 1 : 0;
+static void (*prefill_kernel(int sched))(FwdParams) {
+  return sched == kSchedSplit    ? attn_fwd_kernel<D, BF16, kSchedSplit>
+         : sched == kSchedHalves ? attn_fwd_kernel<D, BF16, kSchedHalves>
+                                 : attn_fwd_kernel<D, BF16, kSchedPlain>;
+}
+
+template <int D, bool BF16>
+static bool prefill_kernel_ready(int dev, int sched) {
+  static std::once_flag once[3][64];
+  static bool ok[3][64];
+  auto kern = prefill_kernel<D, BF16>(sched);
+  const int k = sched;
   std::call_once(once[k][dev], [&] {
     cudaFuncAttributes fa;
     ok[k][dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -192,10 +199,9 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.window = s.window;
   // An item holds up to two query tiles: two heads of one GQA group at the
   // same rows when the group size is even (they share every K/V load);
-  // otherwise row tiles of one head, paired so that the longest item is as
-  // short as possible: one tile per item when every tile can have an SM,
-  // mirrored pairs (r, n-1-r) for a causal call that fits one wave,
-  // consecutive pairs (2r, 2r+1) otherwise.
+  // otherwise one tile whose K/V tiles the two softmax warpgroups split, when
+  // the tiles are few; consecutive row tiles (2r, 2r+1) of one head
+  // otherwise.
   const int sms_now = device_sm_count();
   const long long ntiles = (s.Nq + kBM - 1) / kBM;
   const size_t split_bytes = ws ? split_plan_bytes(s, sms_now) : 0;
@@ -208,12 +214,15 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   } else if (p.group % 2 == 0) {
     p.pair_mode = kPairHeads;
     p.n_row_blocks = static_cast<int>(ntiles);
-  } else if (zq * ntiles <= sms_now) {
-    p.pair_mode = kPairSingle;
+  } else if (zq * ntiles <= sms_now || (s.causal && zq * ((ntiles + 1) / 2) <= sms_now)) {
+    // Few tiles (one wave of single tiles, or causal pairs that fit one
+    // wave): one tile per item.  When the longest tile has at least 4 K/V
+    // tiles, the two softmax warpgroups split them, so that no warpgroup
+    // idles while a long tile runs; shorter ones do not repay the merge.
+    int beg = 0, end = 0;
+    tile_range(p, static_cast<int>((ntiles - 1) * kBM), beg, end);
+    p.pair_mode = (end - beg >= 4) ? kPairHalves : kPairSingle;
     p.n_row_blocks = static_cast<int>(ntiles);
-  } else if (s.causal && zq * ((ntiles + 1) / 2) <= sms_now) {
-    p.pair_mode = kPairMirror;
-    p.n_row_blocks = static_cast<int>((ntiles + 1) / 2);
   } else {
     p.pair_mode = kPairRows;
     p.n_row_blocks = static_cast<int>((ntiles + 1) / 2);
@@ -262,10 +271,11 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
 
-  auto kern = split ? attn_fwd_kernel<D, BF16, true> : attn_fwd_kernel<D, BF16, false>;
+  const int sched = split ? kSchedSplit : (p.pair_mode == kPairHalves ? kSchedHalves : kSchedPlain);
+  auto kern = prefill_kernel<D, BF16>(sched);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (!prefill_kernel_ready<D, BF16>(dev, split)) return ATTN_ERR_UNSUPPORTED;
+  if (!prefill_kernel_ready<D, BF16>(dev, sched)) return ATTN_ERR_UNSUPPORTED;
   const int grid = split ? split_ctas : static_cast<int>(std::min<long long>(items, sms_now));
   if (grid <= 0) return ATTN_ERR_CUDA;
   if (launch_pdl(kern, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)

@@ -100,7 +100,8 @@ struct FwdCfg {
   // barriers: qfull[2][QB], qfree[2][QB], kvfull[NS], kvempty[NS],
   //           sfull[2], ofinal[2], drain[2], pvdone[2]
   static constexpr int kNumBars = 4 * kQBufs + 2 * kStages + 8;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int kOffMerge = ((kOffBar + kNumBars * 8 + 16) + 15) / 16 * 16;  // float2 (m, l)[128]
+  static constexpr int kSmemBytes = kOffMerge + kBM * 8 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns of tile t.  d = 64: S [256t, +128), P [256t + 128, +64) and
   // O [256t + 192, +64): with P apart from S, the Q K^T of the next key block
@@ -200,11 +201,12 @@ ATTN_HD void tile_range(const FwdParams &p, int row0, int &beg, int &end) {
 //   kPairHeads   two query heads of one GQA group at the same 128 rows: each
 //                K/V tile load serves both (group size even)
 //   kPairRows    row tiles 2r and 2r+1 of one head (the default otherwise)
-//   kPairMirror  row tiles r and n-1-r of one head: with a causal mask the
-//                two lengths add up to about the same for every item, which
-//                shortens the longest item when all items run in one wave
-//   kPairSingle  one row tile per item: when every tile can have its own SM
-enum PairMode : int { kPairRows = 0, kPairHeads = 1, kPairMirror = 2, kPairSingle = 3 };
+//   kPairSingle  one row tile per item: few tiles, each of at most 3 K/V tiles
+//   kPairHalves  one row tile per item, its K/V tiles split between the two
+//                tiles of the item (tile 0 the first half, tile 1 the rest),
+//                loaded into the ring interleaved and merged at the end: both
+//                softmax warpgroups work on every item (few, longer tiles)
+enum PairMode : int { kPairRows = 0, kPairHeads = 1, kPairSingle = 2, kPairHalves = 3 };
 
 ATTN_HD Item decode_item(const FwdParams &p, int item) {
   Item it;
@@ -226,14 +228,10 @@ ATTN_HD Item decode_item(const FwdParams &p, int item) {
       const int rb = p.n_row_blocks - 1 - idx;
       it.row0[0] = rb * 2 * kBM;
       it.row0[1] = rb * 2 * kBM + kBM;
-    } else if (p.pair_mode == kPairMirror) {
-      const int ntiles = (p.Nq + kBM - 1) / kBM;
-      const int a = idx, c = ntiles - 1 - idx;  // a <= c
-      it.row0[0] = a * kBM;
-      it.row0[1] = (c > a) ? c * kBM : p.Nq;  // the middle tile of an odd count goes alone
     } else {
       it.row0[0] = (p.n_row_blocks - 1 - idx) * kBM;
-      it.row0[1] = p.Nq;  // no second tile
+      // kPairSingle: no second tile; kPairHalves: the same rows
+      it.row0[1] = (p.pair_mode == kPairHalves) ? it.row0[0] : p.Nq;
     }
   }
   it.ubeg = 1 << 30;
@@ -251,9 +249,35 @@ ATTN_HD Item decode_item(const FwdParams &p, int item) {
     it.obeg[t] = it.beg[t];
     it.oend[t] = it.end[t];
   }
+  if (p.pair_mode == kPairHalves && it.valid[0]) {
+    // the first half of the K/V tiles (rounded up) to tile 0, the rest to tile 1
+    const int mid = it.beg[0] + (it.end[0] - it.beg[0] + 1) / 2;
+    it.end[0] = it.oend[0] = mid;
+    it.beg[1] = it.obeg[1] = mid;
+    it.valid[1] = it.exists[1] = mid < it.end[1];
+  }
   it.iubeg = it.ubeg;
   it.iuend = it.uend;
   return it;
+}
+
+// K/V tile held by ring position k of an item (k from 0).  The ring is loaded
+// in the item's union order, except under kPairHalves, where the two tiles'
+// ranges alternate: tile 0's i-th, tile 1's i-th, ..., then the rest of the
+// longer one (tile 0's; tile 1 has at most as many).
+template <bool kHalves>
+ATTN_HD int ring_block(const Item &it, int k) {
+  if (!kHalves || !it.valid[1]) return it.ubeg + k;
+  const int n1 = it.end[1] - it.beg[1];
+  if (k < 2 * n1) return (k & 1) ? it.beg[1] + (k >> 1) : it.beg[0] + (k >> 1);
+  return it.beg[0] + (k - n1);
+}
+// Ring position of tile t's i-th K/V tile of the item.
+template <bool kHalves>
+ATTN_HD int ring_pos(const Item &it, int t, int i) {
+  if (!kHalves || !it.valid[1]) return (t ? it.beg[1] : it.beg[0]) - it.ubeg + i;
+  const int n1 = it.end[1] - it.beg[1];
+  return (i < n1) ? 2 * i + t : n1 + i;
 }
 
 // Restrict an item to the K/V tiles [iubeg + s0, iubeg + s1) of its union
@@ -354,12 +378,21 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&sr)[kBN], float2 sl2x
 constexpr uint32_t kBarP = 1, kBarSRead = 3, kBarHandoffThreads = 128 + 32;
 // Named barrier of one softmax warpgroup alone: its O tile is staged.
 constexpr uint32_t kBarOStaged = 5;
+// kPairHalves merge, both softmax warpgroups (256 threads): tile 0's (m, l)
+// and final O are ready (tile 0 arrives, tile 1 syncs); tile 1 has read them
+// (tile 1 arrives, tile 0 syncs).
+constexpr uint32_t kBarHalfReady = 7, kBarHalfRead = 8, kBarHalvesThreads = 256;
 
 
-// kSplit: the stream-K schedule (FwdParams::split_at); the plain schedule
-// otherwise, compiled without any of the split's code.
-template <int D, bool BF16, bool kSplit>
+// Schedules, one kernel each: the plain item list, the stream-K split
+// (FwdParams::split_at) and the kPairHalves items; each is compiled without
+// the others' code.
+enum Sched : int { kSchedPlain = 0, kSchedSplit = 1, kSchedHalves = 2 };
+
+template <int D, bool BF16, int kSched>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  constexpr bool kSplit = kSched == kSchedSplit;
+  constexpr bool kHalves = kSched == kSchedHalves;
   using C = FwdCfg<D>;
   constexpr int NS = C::kStages;
   constexpr int QB = C::kQBufs;
@@ -457,7 +490,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           nq[t] = k + 1;
         }
         const int zkv = it.b * p.Hkv + it.kvh;
-        for (int j = it.ubeg; ok && j < it.uend; ++j) {
+        for (int k = 0; ok && k < it.uend - it.ubeg; ++k) {
+          const int j = ring_block<kHalves>(it, k);  // K/V tile of ring position k
           const int c = ckv, s = c % NS;
           if (c >= NS && !mbar_wait_warp(bKVempty(s), ((c / NS) - 1) & 1, wc, kErrWaitKVEmpty)) {
             ok = false;
@@ -556,13 +590,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         const bool tvalid = t ? it.valid[1] : it.valid[0];
         const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
         const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
-        const int c0 = ckv - it.ubeg;  // ring slot of K/V block j is c0 + j
-        for (int j = it.ubeg; j < tbeg; ++j) pass_slot(c0 + j);
+        const int base = ckv;  // ring slot of the item's first position
+        const int npos = it.uend - it.ubeg;
+        // positions before this tile's first K/V tile are passed
+        const int first_pos = tvalid ? ring_pos<kHalves>(it, t, 0) : npos;
+        for (int k = 0; k < first_pos; ++k) pass_slot(base + k);
+        int next_pos = first_pos;
         if (tvalid) {
           const int qbuf = nq % QB;
           if (ok) ok = mbar_wait_warp(bQfull(t, qbuf), (nq / QB) & 1, wc, kErrWaitQ);
           for (int j = tbeg; j < tend; ++j) {
-            const int c = c0 + j;
+            // positions of the other tile between this one's are passed
+            const int pos_j = ring_pos<kHalves>(it, t, j - tbeg);
+            for (int k = next_pos; k < pos_j; ++k) pass_slot(base + k);
+            next_pos = pos_j + 1;
+            const int c = base + pos_j;
             if constexpr (C::kSeparateP) {
               // S of the previous block read -> Q K^T of block j; then P V of
               // the previous block once its P is written.
@@ -588,8 +630,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           issue_pv();
           nq++;
         }
-        for (int j = tend; j < it.uend; ++j) pass_slot(c0 + j);
-        ckv = c0 + it.uend;
+        for (int k = next_pos; k < npos; ++k) pass_slot(base + k);
+        ckv = base + npos;
       }
       // Drain every MMA this warp issued before TMEM can be released (the
       // commit comes from the lane that issued them).
@@ -640,6 +682,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       const int pos = trow0 + row + (p.Nk - p.Nq);  // absolute position of this query row
       const int p0 = trow0 + (p.Nk - p.Nq);
       const int p1 = min(trow0 + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
+      // kPairHalves with both halves: tile 0 hands its half to tile 1
+      const bool half_out = kHalves && t == 0 && it.valid[1];
+      const bool half_merge = kHalves && t == 1;
       float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
       float l = 0.f;        // running sum of exp2(s * sl2 - m), fp32
       for (int j = tbeg; j < tend; ++j) {
@@ -778,14 +823,44 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           }
         }
       }
-      const float a_own = (m == -INFINITY) ? 0.f : ex2_approx(m - mf);  // 1 unless merged
-      const float inv = part_out ? 1.f : ((lf > 0.f) ? 1.f / lf : 0.f);
-      if (ok && live_row && p.lse != nullptr && !part_out)
+      float a_own = (m == -INFINITY) ? 0.f : ex2_approx(m - mf);  // 1 unless merged
+      float inv = part_out ? 1.f : ((lf > 0.f) ? 1.f / lf : 0.f);
+      if (ok && live_row && p.lse != nullptr && !part_out && !half_out && !half_merge)
         p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
             ((lf > 0.f) ? mf + log2f(lf) : -INFINITY) * 0.69314718055994530942f;
       const int qbuf = nfin % QB;  // this item's Q buffer (the MMA warp counts items the same way)
       ok = ok && mbar_wait_warp(bOfinal(t), nfin & 1, wc, kErrWaitOFinal);
       nfin++;
+      // kPairHalves: tile 0's (m, l) go through shared memory, its final O is
+      // read by tile 1 straight from TMEM (same lanes: same rows)
+      float2 *half_ml = reinterpret_cast<float2 *>(smem + C::kOffMerge);
+      float a_half = 0.f;  // weight of tile 0's half in tile 1's merge
+      if (half_out) {
+        half_ml[row] = make_float2(m, l);
+        tc_fence_before();
+        named_bar_arrive(kBarHalfReady, kBarHalvesThreads);
+        named_bar_sync(kBarHalfRead, kBarHalvesThreads);  // tile 1 has read O_0: it may be overwritten
+      }
+      if (half_merge) {
+        named_bar_sync(kBarHalfReady, kBarHalvesThreads);
+        tc_fence_after();
+        const float2 h = half_ml[row];
+        mf = fmaxf(m, h.x);
+        a_own = (m == -INFINITY) ? 0.f : ex2_approx(m - mf);
+        a_half = (h.x == -INFINITY) ? 0.f : ex2_approx(h.x - mf);
+        lf = l * a_own + h.y * a_half;
+        inv = (lf > 0.f) ? 1.f / lf : 0.f;
+        if (ok && live_row && p.lse != nullptr)
+          p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
+              ((lf > 0.f) ? mf + log2f(lf) : -INFINITY) * 0.69314718055994530942f;
+      }
+      const uint32_t ocol_half = tmem + lane_off + C::kColO0;  // O of tile 0
+      auto half_read_done = [&]() {
+        if (half_merge) {
+          tc_fence_before();
+          named_bar_arrive(kBarHalfRead, kBarHalvesThreads);
+        }
+      };
       // 32 columns of this row's output before the 1/l: O_t from TMEM, plus
       // the other pieces' partials when merging
       auto out_chunk = [&](int cc, float (&v)[32]) {
@@ -793,6 +868,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         tmem_ld32(ocol + cc * 32, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if (half_merge) {
+          uint32_t r0[32];
+          tmem_ld32(ocol_half + cc * 32, r0);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = fmaf(__uint_as_float(r0[i]), a_half, v[i] * a_own);
+        }
         if (merge_in) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= a_own;
@@ -807,7 +888,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           }
         }
       };
-      if (part_out) {
+      if (half_out) {
+        if constexpr (C::kStoreOViaSmem) o_pending = qbuf;  // no store read the Q buffer
+      } else if (part_out) {
         // partial O (not normalised) and (m, l) of each row, then the flag:
         // the barrier orders every thread's writes before the one release
         if (ok) {
@@ -850,6 +933,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           }
           fence_proxy_async_smem();  // the rows are visible to the TMA store
         }
+        half_read_done();
         named_bar_sync(kBarOStaged + t, 128);
         if (ok && quad == 0 && lane == 0) {
           tma_store_3d(&p.tmO, stage, 0, trow0, tbh);
@@ -857,26 +941,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         }
         __syncwarp();
         o_pending = qbuf;
-      } else if (ok) {
-        tc_fence_after();
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                        (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
+      } else {
+        if (ok) {
+          tc_fence_after();
+          uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                          (static_cast<size_t>(tbh) * p.Nq + (live_row ? grow : 0)) * (D * 2);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float v[32];
-          out_chunk(cc, v);
-          if (live_row) {
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float v[32];
+            out_chunk(cc, v);
+            if (live_row) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w;
-              w.x = pack2<BF16>(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv);
-              w.y = pack2<BF16>(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv);
-              w.z = pack2<BF16>(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv);
-              w.w = pack2<BF16>(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv);
-              *reinterpret_cast<uint4 *>(orow + cc * 64 + q * 16) = w;
+              for (int q = 0; q < 4; ++q) {
+                uint4 w;
+                w.x = pack2<BF16>(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv);
+                w.y = pack2<BF16>(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv);
+                w.z = pack2<BF16>(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv);
+                w.w = pack2<BF16>(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv);
+                *reinterpret_cast<uint4 *>(orow + cc * 64 + q * 16) = w;
+              }
             }
           }
         }
+        half_read_done();
       }
       // The next item's first P V (accumulate = 0) overwrites O_t; it is
       // issued only after the next P barrier, which these warps reach after
