@@ -73,7 +73,7 @@ struct FwdParams {
   FastDiv fd_group;  // / group
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
-  // Stream-K split (the kSplit kernel): the items, in order, form one
+  // Stream-K split (the kSchedSplit kernel): the items, in order, form one
   // sequence of K/V tile steps (each item its union range); CTA c takes the
   // steps from split_at[c] to split_at[c + 1] (x = item, y = step within the
   // item).  An item cut between CTAs is finished by the CTA holding its first
@@ -131,9 +131,6 @@ constexpr int kLaunchRegs = 168;
 constexpr uint32_t kRegsWG0 = 72, kRegsSoftmax = 216;
 static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= 384 * kLaunchRegs, "register split");
 
-__device__ __forceinline__ bool key_live(int key, int pos, int Nk, int causal, int window) {
-  return key < Nk && (!causal || key <= pos) && (window <= 0 || pos - key < window);
-}
 
 // Bounded wait that ignores the abort flag: used only to drain our own
 // asynchronous copies / MMAs, which always complete.
@@ -705,9 +702,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
                                  (p.window > 0 && key0 <= p1 - p.window);
           if (need_mask) {
+            // The row's live keys are one interval: below Nk, not after the
+            // row (causal), within the window.  [lo, hi) relative to key0.
+            const int hi = min(p.Nk, p.causal ? pos + 1 : p.Nk) - key0;
+            const int lo = (p.window > 0) ? pos - p.window + 1 - key0 : -1;
 #pragma unroll
             for (int cc = 0; cc < kBN; ++cc)
-              if (!key_live(key0 + cc, pos, p.Nk, p.causal, p.window)) sr[cc] = 0xff800000u;  // -inf
+              if (cc >= hi || cc < lo) sr[cc] = 0xff800000u;  // -inf
           }
           const bool first = (j == tbeg);
           // Separate P: P_t and O_t are free once the P V of block j-1 has
