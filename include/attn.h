@@ -129,6 +129,26 @@ size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * path.  No device work. */
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace);
 
+/* The prefill kernel's schedule for these sizes, without device work: what
+ * attn_fwd_ex would launch on a device of `sms` SMs (FlashAttention-2,
+ * "Parallelism": query tiles of 128 rows as independent units, each walking
+ * its live K/V tiles of 128 keys).  Only for shapes that take a prefill path
+ * (ATTN_PATH_PREFILL or ATTN_PATH_PREFILL_SPLIT); returns -1 for invalid
+ * sizes, a shape of another path or sms <= 0.
+ *   info (HOST, 4 ints, written): grid (CTAs), schedule (0 one tile pass per
+ *     item, 1 work split by K/V tiles, 2 two warpgroups on one tile's
+ *     halves), item shape (0 consecutive row tiles, 1 two heads of a group,
+ *     2 one tile, 3 one tile in halves), item count.
+ *   visits (HOST, 6 ints per visit, written up to max_visits visits): one
+ *     visit per (query tile, K/V tile) product that a softmax warpgroup
+ *     computes, in each CTA's order and, within a piece of work, in the
+ *     order the K/V ring is loaded: {cta, item, tile slot (0 or 1), b * Hq +
+ *     h, first query row, K/V tile index}.
+ * Returns the number of visits (it may exceed max_visits: then only the
+ * first max_visits are written). */
+int attn_fwd_prefill_visits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
+                            int with_workspace, int sms, int *info, int *visits, int max_visits);
+
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.

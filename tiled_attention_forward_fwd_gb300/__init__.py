@@ -33,7 +33,7 @@ ATTN_PATH_SPLIT_KV_FUSED = 4
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
-            "attn_fwd_decode_noalloc", "attn_fwd_path"]
+            "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits"]
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_decode_noalloc.restype = ci
         L.attn_fwd_path.argtypes = [ci, ci, ci, ci, ci, ci, ci]
         L.attn_fwd_path.restype = ci
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.attn_fwd_prefill_visits.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ip, ip, ci]
+        L.attn_fwd_prefill_visits.restype = ci
         del fp
         _lib = L
         return _lib
@@ -100,6 +103,25 @@ def attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
 
 def attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, with_workspace) -> int:
     return int(lib().attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, 1 if with_workspace else 0))
+
+
+def attn_fwd_prefill_visits(B, Hq, Hkv, Nq, Nk, d, causal, window, with_workspace, sms):
+    """The prefill schedule without device work: (info, visits) with info =
+    (grid, schedule, item shape, items) and visits an (n, 6) int32 array of
+    (cta, item, tile slot, b * Hq + h, first query row, K/V tile) in launch
+    order; None when the sizes take no prefill path."""
+    import numpy as np
+
+    info = (ctypes.c_int * 4)()
+    args = (B, Hq, Hkv, Nq, Nk, d, int(causal), int(window), 1 if with_workspace else 0, sms)
+    n = lib().attn_fwd_prefill_visits(*args, info, None, 0)
+    if n < 0:
+        return None
+    visits = np.zeros((max(n, 1), 6), dtype=np.int32)
+    got = lib().attn_fwd_prefill_visits(*args, info, visits.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n)
+    if got != n:
+        raise RuntimeError("attn_fwd_prefill_visits: visit count changed between calls")
+    return tuple(info), visits[:n]
 
 
 def attn_fwd_host(Qh, Kh, Vh, Oh, LSEh, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, dev_buf,

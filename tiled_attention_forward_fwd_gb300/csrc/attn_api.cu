@@ -173,22 +173,12 @@ static bool prefill_kernel_ready(int dev, int sched) {
   return ok[k][dev];
 }
 
-template <int D, bool BF16>
-static attn_status_t launch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
-                                   const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream) {
-  using Cfg = FwdCfg<D>;
-  FwdParams p;
-  std::memset(&p, 0, sizeof(p));
+// The schedule of a prefill call on `sms_now` SMs: item shape, item count
+// and divisors in p, the kernel (kSched*) and its grid; with `split`, the
+// stream-K split points too.  Host only, no device work.  False when the
+// item count overflows.
+static bool prefill_schedule(const Shape &s, bool split, int sms_now, FwdParams &p, int &sched, int &grid) {
   const long long zq = static_cast<long long>(s.B) * s.Hq;
-  const long long zk = static_cast<long long>(s.B) * s.Hkv;
-  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16) ||
-      !make_map(&p.tmV, V, D, s.Nk, zk, BF16) || (Cfg::kStoreOViaSmem && !make_map(&p.tmO, O, D, s.Nq, zq, BF16)))
-    return ATTN_ERR_CUDA;
-  int *status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
-  p.O = O;
-  p.lse = LSE;
-  p.status = status;
   p.B = s.B;
   p.Hq = s.Hq;
   p.Hkv = s.Hkv;
@@ -202,11 +192,7 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   // otherwise one tile whose K/V tiles the two softmax warpgroups split, when
   // the tiles are few; consecutive row tiles (2r, 2r+1) of one head
   // otherwise.
-  const int sms_now = device_sm_count();
   const long long ntiles = (s.Nq + kBM - 1) / kBM;
-  const size_t split_bytes = ws ? split_plan_bytes(s, sms_now) : 0;
-  if (split_bytes > 0 && (ws_bytes < split_bytes || !aligned16(ws))) return ATTN_ERR_INVALID_ARG;
-  const bool split = split_bytes > 0;
   if (split) {
     // both tiles of every item busy: heads of a group, else row pairs
     p.pair_mode = (p.group % 2 == 0) ? kPairHeads : kPairRows;
@@ -229,7 +215,7 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   }
   const long long slots = (p.pair_mode == kPairHeads) ? zq / 2 : zq;
   const long long items = slots * p.n_row_blocks;
-  if (items > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (items > 0x7fffffffLL) return false;
   p.n_slots = static_cast<int>(slots);
   p.n_items = static_cast<int>(items);
   p.fd_slots = fastdiv_make(static_cast<uint32_t>(p.n_slots));
@@ -258,7 +244,35 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
       p.split_at[c] = make_int2(item, static_cast<int>(target - before));
     }
     p.split_at[split_ctas] = make_int2(p.n_items, 0);
+  }
+  sched = split ? kSchedSplit : (p.pair_mode == kPairHalves ? kSchedHalves : kSchedPlain);
+  grid = split ? split_ctas : static_cast<int>(std::min<long long>(items, sms_now));
+  return true;
+}
 
+template <int D, bool BF16>
+static attn_status_t launch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                   const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream) {
+  using Cfg = FwdCfg<D>;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long zq = static_cast<long long>(s.B) * s.Hq;
+  const long long zk = static_cast<long long>(s.B) * s.Hkv;
+  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16) ||
+      !make_map(&p.tmV, V, D, s.Nk, zk, BF16) || (Cfg::kStoreOViaSmem && !make_map(&p.tmO, O, D, s.Nq, zq, BF16)))
+    return ATTN_ERR_CUDA;
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  p.O = O;
+  p.lse = LSE;
+  p.status = status;
+  const int sms = device_sm_count();
+  const size_t split_bytes = ws ? split_plan_bytes(s, sms) : 0;
+  if (split_bytes > 0 && (ws_bytes < split_bytes || !aligned16(ws))) return ATTN_ERR_INVALID_ARG;
+  int sched = kSchedPlain, grid = 0;
+  if (!prefill_schedule(s, split_bytes > 0, sms, p, sched, grid)) return ATTN_ERR_INVALID_ARG;
+  if (sched == kSchedSplit) {
+    const int split_ctas = grid;
     unsigned tok = ++g_split_token;
     if (tok == 0) tok = ++g_split_token;
     p.token = tok;
@@ -271,12 +285,10 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
 
-  const int sched = split ? kSchedSplit : (p.pair_mode == kPairHalves ? kSchedHalves : kSchedPlain);
   auto kern = prefill_kernel<D, BF16>(sched);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
   if (!prefill_kernel_ready<D, BF16>(dev, sched)) return ATTN_ERR_UNSUPPORTED;
-  const int grid = split ? split_ctas : static_cast<int>(std::min<long long>(items, sms_now));
   if (grid <= 0) return ATTN_ERR_CUDA;
   if (launch_pdl(kern, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -592,6 +604,56 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
   if (with_workspace && dp.bytes > 0) return dp.fused ? ATTN_PATH_SPLIT_KV_FUSED : ATTN_PATH_SPLIT_KV;
   if (with_workspace && split_plan_bytes(s, device_sm_count()) > 0) return ATTN_PATH_PREFILL_SPLIT;
   return ATTN_PATH_PREFILL;
+}
+
+int attn_fwd_prefill_visits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
+                            int with_workspace, int sms, int *info, int *visits, int max_visits) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128) ||
+      sms <= 0 || window < 0 || (window > 0 && !causal) || (causal && Nq > Nk) || info == nullptr ||
+      (max_visits > 0 && visits == nullptr))
+    return -1;
+  Shape s{B, Hq, Hkv, Nq, Nk, d, causal, window, 1.f, ATTN_DTYPE_FP16};
+  if (short_path(s)) return -1;
+  // with a workspace, small query groups take the split-KV path (on any
+  // device where its kernel fits)
+  if (with_workspace && static_cast<long long>(Hq / Hkv) * Nq <= kDecMaxRows && static_cast<long long>(B) * Hkv <= 65535)
+    return -1;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  int sched = kSchedPlain, grid = 0;
+  if (!prefill_schedule(s, with_workspace && split_plan_bytes(s, sms) > 0, sms, p, sched, grid)) return -1;
+  info[0] = grid;
+  info[1] = sched;
+  info[2] = p.pair_mode;
+  info[3] = p.n_items;
+  // the kernel's own walk: per CTA its pieces, per piece the ring positions
+  // in load order, per position the tiles that take its K/V tile
+  long long n = 0;
+  for (int c = 0; c < grid; ++c) {
+    const int np = sched == kSchedSplit ? num_pieces<true>(p, c, grid) : num_pieces<false>(p, c, grid);
+    for (int k = 0; k < np; ++k) {
+      Item it;
+      const bool got = sched == kSchedSplit ? piece_at<true>(p, c, grid, k, it) : piece_at<false>(p, c, grid, k, it);
+      if (!got) continue;
+      for (int pos = 0; pos < it.uend - it.ubeg; ++pos) {
+        const int j = sched == kSchedHalves ? ring_block<true>(it, pos) : ring_block<false>(it, pos);
+        for (int t = 0; t < 2; ++t) {
+          if (!it.valid[t] || j < it.beg[t] || j >= it.end[t]) continue;
+          if (n < max_visits) {
+            int *v = visits + 6 * n;
+            v[0] = c;
+            v[1] = it.item;
+            v[2] = t;
+            v[3] = it.bh[t];
+            v[4] = it.row0[t];
+            v[5] = j;
+          }
+          ++n;
+        }
+      }
+    }
+  }
+  return n > 0x7fffffffLL ? -1 : static_cast<int>(n);
 }
 
 size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_lse) {

@@ -292,36 +292,33 @@ ATTN_HD void clip_item(Item &it, int s0, int s1) {
   }
 }
 
-// Items are handed to the persistent CTAs in passes of gridDim.x, alternating
+// Items are handed to the g persistent CTAs in passes of g, alternating
 // direction ("snake"): with items sorted longest first, every CTA gets a
-// similar total.  Returns the m-th item of this CTA (>= n_items: none).
-__device__ __forceinline__ int item_of(int m) {
-  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  return m * g + ((m & 1) ? (g - 1 - c) : c);
-}
+// similar total.  Returns the m-th item of CTA c (>= n_items: none).
+ATTN_HD int item_of(int m, int c, int g) { return m * g + ((m & 1) ? (g - 1 - c) : c); }
 
-// Number of work pieces of this CTA: passes over the item list, or the
+// Number of work pieces of CTA c of g: passes over the item list, or the
 // items that its stream-K range touches.
 template <bool kSplit>
-__device__ __forceinline__ int num_pieces(const FwdParams &p) {
-  if constexpr (!kSplit) return (p.n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-  const int2 s = p.split_at[blockIdx.x], e = p.split_at[blockIdx.x + 1];
+ATTN_HD int num_pieces(const FwdParams &p, int c, int g) {
+  if constexpr (!kSplit) return (p.n_items + g - 1) / g;
+  const int2 s = p.split_at[c], e = p.split_at[c + 1];
   const int last = (e.y > 0) ? e.x : e.x - 1;  // last item touched
   if (s.x > last || (s.x == e.x && s.y >= e.y)) return 0;
   return last - s.x + 1;
 }
 
-// The k-th piece of this CTA's work; false when there is none (the last pass
-// over the item list may be short).
+// The k-th piece of the work of CTA c of g; false when there is none (the
+// last pass over the item list may be short).
 template <bool kSplit>
-__device__ __forceinline__ bool piece_at(const FwdParams &p, int k, Item &it) {
+ATTN_HD bool piece_at(const FwdParams &p, int c, int g, int k, Item &it) {
   if constexpr (!kSplit) {
-    const int item = item_of(k);
+    const int item = item_of(k, c, g);
     if (item >= p.n_items) return false;
     it = decode_item(p, item);
     return true;
   }
-  const int2 s = p.split_at[blockIdx.x], e = p.split_at[blockIdx.x + 1];
+  const int2 s = p.split_at[c], e = p.split_at[c + 1];
   const int item = s.x + k;
   it = decode_item(p, item);
   clip_item(it, k == 0 ? s.y : 0, item == e.x ? e.y : (1 << 30));
@@ -464,10 +461,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       int nq[2] = {0, 0};
       int ckv = 0;
       bool ok = true;
-      const int npieces = num_pieces<kSplit>(p);
+      const int npieces = num_pieces<kSplit>(p, blockIdx.x, gridDim.x);
       for (int pk = 0; ok && pk < npieces; ++pk) {
         Item it;
-        if (!piece_at<kSplit>(p, pk, it)) continue;
+        if (!piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, it)) continue;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || !it.valid[t]) continue;
@@ -580,10 +577,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         }
         pending = false;
       };
-      const int npieces = num_pieces<kSplit>(p);
+      const int npieces = num_pieces<kSplit>(p, blockIdx.x, gridDim.x);
       for (int pk = 0; pk < npieces; ++pk) {
         Item it;
-        if (!piece_at<kSplit>(p, pk, it)) continue;
+        if (!piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, it)) continue;
         const bool tvalid = t ? it.valid[1] : it.valid[0];
         const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
         const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
@@ -665,10 +662,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       __syncwarp();
       o_pending = -1;
     };
-    const int npieces = num_pieces<kSplit>(p);
+    const int npieces = num_pieces<kSplit>(p, blockIdx.x, gridDim.x);
     for (int pk = 0; pk < npieces; ++pk) {
       Item it;
-      if (!piece_at<kSplit>(p, pk, it)) continue;
+      if (!piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, it)) continue;
       // this warpgroup's tile, as scalars (t is not a compile-time index)
       const bool tvalid = t ? it.valid[1] : it.valid[0];
       if (!tvalid) continue;
@@ -792,7 +789,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       Item ie{};
       bool part_out = false, merge_in = false;
       if constexpr (kSplit) {
-        piece_at<kSplit>(p, pk, ie);
+        piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, ie);
         part_out = ie.ubeg > ie.iubeg;
         merge_in = ie.ubeg == ie.iubeg && ie.uend < ie.iuend;
       }
