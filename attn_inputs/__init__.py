@@ -103,7 +103,7 @@ def normal_tensor(seed: int, shape, dtype: str, scale: float = 1.0) -> torch.Ten
 
 
 def seed_for(config_id: int, layer: int, which: str) -> int:
-    return 1000 * config_id + 10 * layer + {"Q": 0, "K": 1, "V": 2}[which]
+    return 1000 * config_id + 10 * layer + {"Q": 0, "K": 1, "V": 2, "L": 3, "P": 4}[which]
 
 
 @dataclass(frozen=True)
@@ -134,6 +134,90 @@ def make_qkv(shape: AttnShape, config_id: int = 0, layer: int = 0):
                       scale=shape.key_scale)
     v = normal_tensor(seed_for(config_id, layer, "V"), (shape.B, shape.Hkv, shape.Nk, shape.d), shape.dtype)
     return q, k, v
+
+
+@dataclass(frozen=True)
+class PagedShape:
+    """One call on a paged K/V cache: Q,O (B,Hq,Nq,d); K,V pools
+    (num_pages,Hkv,page_size,d); a page table (B,max_pages) and a length per
+    request.  ``lens`` fixes the lengths; otherwise they are drawn uniformly
+    from [min_len, max_seq_len]."""
+
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    max_seq_len: int
+    d: int
+    page_size: int = 16
+    dtype: str = "bf16"
+    causal: bool = True
+    window: int = 0
+    sm_scale: float | None = None
+    lens: tuple | None = None
+    min_len: int = 1
+    spare_pages: int = 0  # pool pages no request owns
+
+    @property
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(self.d)
+
+    @property
+    def max_pages(self) -> int:
+        return -(-self.max_seq_len // self.page_size)
+
+
+def _uniform_ints(seed: int, n: int, lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
+    """n integers, the k-th uniform on [lo_k, hi_k] (floor of a 53-bit uniform)."""
+    u = uniform53(splitmix64(seed, 0, n))
+    return (lo + np.floor(u * (hi - lo + 1)).astype(np.int64)).astype(np.int64)
+
+
+def make_paged(shape: PagedShape, config_id: int = 0, layer: int = 0, poison: bool = True):
+    """Seeded paged inputs: ``(q, k_pool, v_pool, block_table, seq_lens)`` as
+    CPU tensors (int32 for the table and lengths).
+
+    Each request gets ceil(len / page_size) pages.  The pool is shuffled
+    (Fisher-Yates, Knuth TAOCP vol. 2, Algorithm 3.4.2P, driven by the
+    stream above), so a request's pages are scattered, as in a fragmented
+    cache.  Table entries past a request's pages are -1.  With ``poison``,
+    every pool slot that no request owns (spare pages, and slots past a
+    request's length in its last page) holds NaN, so that any read of one
+    shows in the result."""
+    B, ps = shape.B, shape.page_size
+    if shape.lens is not None:
+        lens = np.asarray(shape.lens, dtype=np.int64)
+        if lens.shape != (B,):
+            raise ValueError("lens must have one entry per request")
+    else:
+        lens = _uniform_ints(seed_for(config_id, layer, "L"), B, np.full(B, shape.min_len),
+                             np.full(B, shape.max_seq_len))
+    pages = -(-lens // ps)
+    num_pages = int(pages.sum()) + shape.spare_pages
+    perm = np.arange(num_pages, dtype=np.int64)
+    if num_pages > 1:
+        idx = np.arange(num_pages - 1, 0, -1)
+        js = _uniform_ints(seed_for(config_id, layer, "P"), num_pages - 1, np.zeros_like(idx), idx)
+        for i, j in zip(idx, js):
+            perm[i], perm[j] = perm[j], perm[i]
+    table = np.full((B, shape.max_pages), -1, dtype=np.int32)
+    owned = np.zeros((num_pages, ps), dtype=bool)
+    nxt = 0
+    for b in range(B):
+        for j in range(int(pages[b])):
+            pg = int(perm[nxt])
+            nxt += 1
+            table[b, j] = pg
+            owned[pg, :min(ps, int(lens[b]) - j * ps)] = True
+    q = normal_tensor(seed_for(config_id, layer, "Q"), (B, shape.Hq, shape.Nq, shape.d), shape.dtype)
+    pool = (num_pages, shape.Hkv, ps, shape.d)
+    k = normal_tensor(seed_for(config_id, layer, "K"), pool, shape.dtype)
+    v = normal_tensor(seed_for(config_id, layer, "V"), pool, shape.dtype)
+    if poison:
+        free = torch.from_numpy(~owned)[:, None, :, None].expand(pool)
+        k = k.masked_fill(free, float("nan"))
+        v = v.masked_fill(free, float("nan"))
+    return q, k, v, torch.from_numpy(table), torch.from_numpy(lens.astype(np.int32))
 
 
 def sha256_of(t: torch.Tensor) -> str:

@@ -57,6 +57,10 @@ def _load():
             lib.oracle_attn_rows.argtypes = [dp, i64p, ctypes.c_long, dp, dp, dp, dp, ci, ci, ci,
                                              ci, ci, ci, ci, ci, ctypes.c_double, ci]
             lib.oracle_attn_rows.restype = ci
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            lib.oracle_attn_paged.argtypes = [dp, dp, dp, i32p, i32p, dp, dp, ci, ci, ci, ci, ci, ci, ci,
+                                              ci, ci, ci, ctypes.c_double, ci]
+            lib.oracle_attn_paged.restype = ci
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -114,4 +118,36 @@ def attention_rows(q_rows, row_ids, k, v, B: int, Hq: int, Nq: int, causal: bool
                                   int(window), scale, int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_attn_rows failed with code {rc}")
+    return o, lse
+
+
+def attention_paged(q, k_pool, v_pool, block_table, seq_lens, causal: bool = False, window: int = 0,
+                    sm_scale: float | None = None, nthreads: int = 0):
+    """fp64 attention over a paged K/V cache.
+
+    q: (B,Hq,Nq,d); k_pool, v_pool: (num_pages,Hkv,page_size,d); block_table:
+    (B,max_pages) int; seq_lens: (B,) int.  Token t of request b is slot
+    t % page_size of pool page block_table[b, t // page_size]; row i of
+    request b sits at position seq_lens[b] - Nq + i.  Returns ``(O, LSE)``
+    as float64 numpy arrays (B,Hq,Nq,d) and (B,Hq,Nq)."""
+    q, kp, vp = _f64(q), _f64(k_pool), _f64(v_pool)
+    if isinstance(block_table, torch.Tensor):
+        block_table = block_table.cpu().numpy()
+    if isinstance(seq_lens, torch.Tensor):
+        seq_lens = seq_lens.cpu().numpy()
+    table = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    B, Hq, Nq, d = q.shape
+    num_pages, Hkv, page_size = kp.shape[0], kp.shape[1], kp.shape[2]
+    if vp.shape != kp.shape or kp.shape[3] != d or table.ndim != 2 or table.shape[0] != B or lens.shape != (B,):
+        raise ValueError("paged oracle: inconsistent shapes")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / float(np.sqrt(d))
+    o = np.empty((B, Hq, Nq, d), dtype=np.float64)
+    lse = np.empty((B, Hq, Nq), dtype=np.float64)
+    rc = _load().oracle_attn_paged(_ptr(q), _ptr(kp), _ptr(vp), _ptr(table, ctypes.c_int32),
+                                   _ptr(lens, ctypes.c_int32), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, d,
+                                   page_size, num_pages, table.shape[1], int(bool(causal)), int(window), scale,
+                                   int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_paged failed with code {rc}")
     return o, lse

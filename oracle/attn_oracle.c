@@ -199,3 +199,81 @@ int oracle_attn_rows(const double *Qrows, const int64_t *row_ids, long n,
   }
   return failed ? ORACLE_ENOMEM : ORACLE_OK;
 }
+
+/* Paged K/V cache (motivation page, "PagedAttention es un problema
+ * distinto": the cache is a pool of fixed-size pages and each request has a
+ * page table naming, in order, the pages that hold its tokens).  The
+ * request's keys are first gathered through its table into a flat array,
+ * then each row is the plain definition above with that request's own key
+ * count n_b = seq_lens[b]:
+ *   token t of request b = pool page table[b * max_pages + t / page_size],
+ *   slot t % page_size;   pool layout (num_pages, Hkv, page_size, d).
+ * Query row i of request b sits at position n_b - Nq + i (step 2 with Nk =
+ * n_b).  Only the first ceil(n_b / page_size) table entries and the first
+ * n_b slots are read.  Returns ORACLE_EINVAL when a length is outside [1,
+ * max_pages * page_size] or a table entry that is read lies outside the
+ * pool. */
+int oracle_attn_paged(const double *Q, const double *Kpool, const double *Vpool,
+                      const int32_t *table, const int32_t *seq_lens, double *O,
+                      double *LSE, int B, int Hq, int Hkv, int Nq, int d,
+                      int page_size, int num_pages, int max_pages, int causal,
+                      int window, double sm_scale, int nthreads) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || d <= 0 || Hq % Hkv != 0)
+    return ORACLE_EINVAL;
+  if (page_size <= 0 || num_pages <= 0 || max_pages <= 0) return ORACLE_EINVAL;
+  if (!(sm_scale > 0.0) || isinf(sm_scale)) return ORACLE_EINVAL;
+  if (!Q || !Kpool || !Vpool || !table || !seq_lens || !O) return ORACLE_EINVAL;
+  long max_len = 0;
+  for (int b = 0; b < B; ++b) {
+    const long n = seq_lens[b];
+    if (n < 1 || n > (long)max_pages * page_size) return ORACLE_EINVAL;
+    for (long j = 0; j < (n + page_size - 1) / page_size; ++j) {
+      const int32_t pg = table[(long)b * max_pages + j];
+      if (pg < 0 || pg >= num_pages) return ORACLE_EINVAL;
+    }
+    if (n > max_len) max_len = n;
+  }
+  const int g = Hq / Hkv;
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)max_len);
+    double *Kh = (double *)malloc(sizeof(double) * (size_t)max_len * d);
+    double *Vh = (double *)malloc(sizeof(double) * (size_t)max_len * d);
+    if (!s || !Kh || !Vh) {
+      failed = 1;
+    } else {
+      /* one (request, query head) per iteration: gather its kv head's keys
+       * and values in token order, then attend each of its Nq rows */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+      for (long bh = 0; bh < (long)B * Hq; ++bh) {
+        const long b = bh / Hq, h = bh % Hq, kvh = h / g;
+        const long n = seq_lens[b];
+        for (long t = 0; t < n; ++t) {
+          const long pg = table[b * max_pages + t / page_size];
+          const long src = ((pg * Hkv + kvh) * page_size + t % page_size) * (long)d;
+          for (long c = 0; c < d; ++c) {
+            Kh[t * d + c] = Kpool[src + c];
+            Vh[t * d + c] = Vpool[src + c];
+          }
+        }
+        for (long i = 0; i < Nq; ++i) {
+          const long r = bh * Nq + i;
+          double lse;
+          attend_one_row(Q + r * d, Kh, Vh, Nq, n, d, i, causal, window, sm_scale,
+                         s, O + r * d, &lse);
+          if (LSE) LSE[r] = lse;
+        }
+      }
+    }
+    free(s);
+    free(Kh);
+    free(Vh);
+  }
+  return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
