@@ -253,7 +253,15 @@ def workload_calls(name: str):
                 (AttnShape(4, 32, 8, 1, 8192, 128, "bf16", True, 0, None), 5, 1)]
     if name == "mha_n64_bw":  # bandwidth-sized sibling of mha_n64: B=512, H=32, N=64, d=64, fp16
         return [(AttnShape(512, 32, 32, 64, 64, 64, "fp16", c, 0, 0.125), 6, int(c)) for c in (False, True)]
+    if name == "paged_decode":
+        # one decode step on a paged cache of 16-token pages, bf16, d=128, GQA 32/8:
+        # the mqa_decode Hkv=8 call with every request at 8192 tokens (same
+        # bytes as the flat call), then a batch of 32 requests of drawn
+        # lengths 512..8192 (the motivation page's batch-32, 8192-token cache)
+        return [(PagedShape(4, 32, 8, 1, 8192, 128, 16, "bf16", True, 0, None, (8192,) * 4), 7, 0),
+                (PagedShape(32, 32, 8, 1, 8192, 128, 16, "bf16", True, 0, None, None, 512), 7, 1)]
     raise KeyError(name)
 
 
-WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw"]
+WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw",
+                  "paged_decode"]

@@ -43,6 +43,8 @@ WORKLOAD_TEXT = {
     "long_prefill": "B=1, Hq=32, Hkv=8, N=32768, d=128, bf16, keys x3, causal",
     "mqa_decode": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16",
     "mha_n64_bw": "MHA forward B=512, H=32, N=64, d=64, fp16, causal in {false,true}",
+    "paged_decode": "decode on a paged cache (16-token pages, shuffled pool), Hq=32, Hkv=8, Nq=1, d=128, bf16: "
+                    "B=4 at 8192 tokens; B=32 at drawn lengths 512..8192",
 }
 KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "attn_short.cuh", "sm103_ptx.cuh", "fastdiv.h"]
 
@@ -174,7 +176,35 @@ def profiled_traffic(workload: str, call_label: str):
 
 # ---------------------------------------------------------------- the workload on the GPU
 def call_label(s) -> str:
+    if isinstance(s, ai.PagedShape):
+        return (f"paged_B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_L{s.max_seq_len}_ps{s.page_size}_d{s.d}_{s.dtype}"
+                f"_c{int(s.causal)}_w{s.window}")
     return (f"B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}_c{int(s.causal)}_w{s.window}")
+
+
+def prepare_paged(shape, cid, layer, device):
+    """One call on a paged cache: seeded pools, table and lengths."""
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    q, k, v, table, lens = ai.make_paged(shape, cid, layer)
+    host = {"q": q, "k": k, "v": v, "table": table, "lens": lens}
+    c = {"shape": shape, "paged": True, **{n + "_host": t for n, t in host.items()},
+         **{n: t.to(device) for n, t in host.items()}}
+    c["o"] = torch.empty_like(c["q"])
+    c["lse"] = torch.empty((shape.B, shape.Hq, shape.Nq), device=device, dtype=torch.float32)
+    c["dtype_code"] = attn.ATTN_DTYPE_BF16 if shape.dtype == "bf16" else attn.ATTN_DTYPE_FP16
+    lens_l = lens.tolist()
+    c["flops"] = acc.paged_flops(shape, lens_l)
+    c["bytes"] = acc.paged_bytes(shape, lens_l)
+    c["label"] = call_label(shape)
+    wsb = attn.attn_fwd_paged_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.max_seq_len, shape.d)
+    c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device)
+    # the split-KV plan of max_seq_len keys (the same plan as a flat call)
+    path = attn.attn_fwd_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.max_seq_len, shape.d, True)
+    c["path"] = path
+    c["kernel"] = "attn_decode_kernel[paged]"
+    c["launches"] = 2 if path == attn.ATTN_PATH_SPLIT_KV else 1
+    return c
 
 
 def prepare(workload: str, device):
@@ -182,6 +212,9 @@ def prepare(workload: str, device):
 
     calls = []
     for shape, cid, layer in ai.workload_calls(workload):
+        if isinstance(shape, ai.PagedShape):
+            calls.append(prepare_paged(shape, cid, layer, device))
+            continue
         q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
         c = {"shape": shape, "q_host": q, "k_host": k, "v_host": v,
              "q": q.to(device), "k": k.to(device), "v": v.to(device)}
@@ -213,6 +246,15 @@ def launch(c, stream_handle):
 
     s = c["shape"]
     ws = c["ws"]
+    if c.get("paged"):
+        st = attn.attn_fwd_paged(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["table"].data_ptr(),
+                                 c["lens"].data_ptr(), c["o"].data_ptr(), c["lse"].data_ptr(), s.B, s.Hq, s.Hkv,
+                                 s.Nq, s.max_seq_len, s.d, s.page_size, c["k"].shape[0], c["table"].shape[1],
+                                 s.causal, s.window, s.scale, c["dtype_code"], ws.data_ptr(), ws.numel(),
+                                 stream_handle)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_fwd_paged failed: {attn.attn_status_string(st)}")
+        return
     st = attn.attn_fwd_ex(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["o"].data_ptr(),
                           c["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale,
                           c["dtype_code"], None if ws is None else ws.data_ptr(),
@@ -304,6 +346,14 @@ def e2e_timing(calls, steps, warmup, device, stream):
     need = 0
     for c in calls:
         s = c["shape"]
+        if c.get("paged"):
+            # the paged call's inputs (pools, table, lengths, Q) are copied
+            # into its device tensors, then attn_fwd_paged runs on them
+            ph = {k: c[k + "_host"].pin_memory() for k in ("q", "k", "v", "table", "lens")}
+            ph["o"] = torch.empty_like(ph["q"]).pin_memory()
+            ph["lse"] = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32).pin_memory()
+            pinned.append(ph)
+            continue
         ph = {k: c[k + "_host"].pin_memory() for k in ("q", "k", "v")}
         ph["o"] = torch.empty_like(ph["q"]).pin_memory()
         ph["lse"] = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32).pin_memory()
@@ -315,11 +365,21 @@ def e2e_timing(calls, steps, warmup, device, stream):
     for c in calls:
         s = c["shape"]
         h2d += (c["q"].numel() + c["k"].numel() + c["v"].numel()) * 2
+        if c.get("paged"):
+            h2d += (c["table"].numel() + c["lens"].numel()) * 4
         d2h += c["o"].numel() * 2 + s.B * s.Hq * s.Nq * 4
 
     def one_step():
         for c, ph in zip(calls, pinned):
             s = c["shape"]
+            if c.get("paged"):
+                with torch.cuda.stream(stream):
+                    for k in ("q", "k", "v", "table", "lens"):
+                        c[k].copy_(ph[k], non_blocking=True)
+                    launch(c, stream.cuda_stream)
+                    ph["o"].copy_(c["o"], non_blocking=True)
+                    ph["lse"].copy_(c["lse"], non_blocking=True)
+                continue
             st = attn.attn_fwd_host(ph["q"].data_ptr(), ph["k"].data_ptr(), ph["v"].data_ptr(), ph["o"].data_ptr(),
                                     ph["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window,
                                     s.scale, c["dtype_code"], base, need, stream.cuda_stream)
@@ -356,15 +416,39 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
     rng = np.random.default_rng(seed)
     prepared = []
     for shape, cid, layer in calls:
+        if isinstance(shape, ai.PagedShape):
+            q, k, v, table, lens = ai.make_paged(shape, cid, layer)
+            prepared.append((shape, q, k.to(torch.float64), v.to(torch.float64), table, lens))
+            continue
         q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
         prepared.append((shape, q.reshape(-1, shape.d), k.to(torch.float64), v.to(torch.float64)))
+
+    def run_paged(shape, q, k, v, table, lens, rows_per_call):
+        # whole requests (all heads and rows), as many as the row budget covers
+        n = min(shape.B, max(1, rows_per_call // (shape.Hq * shape.Nq)))
+        covered.append(n == shape.B)
+        ids = np.sort(rng.choice(shape.B, size=n, replace=False))
+        sel = torch.from_numpy(ids)
+        t0 = time.perf_counter()
+        oracle.attention_paged(q[sel], k, v, table[sel], lens[sel], shape.causal, shape.window, shape.scale)
+        return acc.paged_flops(shape, lens[sel].tolist()), time.perf_counter() - t0
+
+    covered = []  # per call of the last run: the whole call was sampled
 
     def run(rows_per_call):
         flops = 0.0
         t = 0.0
-        for shape, qf, kf, vf in prepared:
+        covered.clear()
+        for shape, *tensors in prepared:
+            if isinstance(shape, ai.PagedShape):
+                f, dt = run_paged(shape, *tensors, rows_per_call)
+                flops += f
+                t += dt
+                continue
+            qf, kf, vf = tensors
             total = shape.B * shape.Hq * shape.Nq
             n = min(total, rows_per_call)
+            covered.append(n == total)
             ids = np.sort(rng.choice(total, size=n, replace=False)).astype(np.int64)
             i = ids % shape.Nq
             pos = shape.Nk - shape.Nq + i
@@ -381,16 +465,22 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
         return flops, t
 
     rows = 16
+    run(rows)  # untimed: OpenMP start-up and first touch of the oracle's scratch
     f, t = run(rows)
-    while t < budget_s / 8 and rows < 1 << 22:
+    while t < budget_s / 8 and rows < 1 << 22 and not all(covered):
         rows *= 4
         f, t = run(rows)
-    if t < budget_s / 2:
+    if t < budget_s / 2 and not all(covered):
         scale = max(1.0, (budget_s * 0.75) / max(t, 1e-6))
         rows = int(rows * scale)
         f, t = run(rows)
-    desc = (f"{rows} seeded random query rows per call of every call in {workload} "
-            f"(capped at the call's rows), fp64 oracle on {cores} OpenMP threads; work = 4*d per live pair")
+    if all(covered):
+        desc = (f"every query row of every call in {workload} (the whole workload fits the sample), "
+                f"fp64 oracle on {cores} OpenMP threads; work = 4*d per live pair")
+    else:
+        desc = (f"{rows} seeded random query rows per call of every call in {workload} "
+                f"(capped at the call's rows; paged calls: whole requests covering that many rows), "
+                f"fp64 oracle on {cores} OpenMP threads; work = 4*d per live pair")
     return f, t, cores, desc
 
 

@@ -62,9 +62,12 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or no sm_100-family GPU */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded internal wait ran out */
-  ATTN_ERR_SCRATCH_LIMIT = 5 /* attn_fwd_decode_noalloc: the shape needs more than the
-                                library's built-in scratch, or does not take the
-                                split-KV path at all */
+  ATTN_ERR_SCRATCH_LIMIT = 5, /* attn_fwd_decode_noalloc: the shape needs more than the
+                                 library's built-in scratch, or does not take the
+                                 split-KV path at all */
+  ATTN_ERR_DEVICE_ARG = 6     /* reported by attn_device_status(): a kernel found a
+                                 device-side argument out of range (attn_fwd_paged:
+                                 a page index or a sequence length) */
 } attn_status_t;
 
 typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
@@ -149,6 +152,50 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
 int attn_fwd_prefill_visits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
                             int with_workspace, int sms, int *info, int *visits, int max_visits);
 
+/* Attention over a paged K/V cache (the motivation page, "PagedAttention es
+ * un problema distinto": the cache is a pool of fixed-size pages, each
+ * request has a page table listing the pages that hold its tokens in order,
+ * and the attention kernel follows the table instead of reading a flat K and
+ * V).  Same result as attn_fwd_ex on each request's K and V gathered into
+ * order, with that request's own key count.  Runs the split-KV kernel, so it
+ * serves GQA groups of at most 32 query rows ((Hq / Hkv) * Nq <= 32: a
+ * decode step, or a few speculative tokens); larger groups return
+ * ATTN_ERR_UNSUPPORTED.
+ *
+ * Q (DEVICE, B x Hq x Nq x d), O (DEVICE, same), LSE (DEVICE fp32, B x Hq x
+ *   Nq, or NULL): as attn_fwd_ex.  Query row i of request b sits at key
+ *   position seq_lens[b] - Nq + i (the causal mask is bottom-right aligned).
+ * K_pages, V_pages (DEVICE, 16-byte aligned): the pools, num_pages x Hkv x
+ *   page_size x d, 16-bit; page p of head h holds page_size consecutive
+ *   tokens of whichever request's table lists p.
+ * block_table (DEVICE int32, B x max_pages_per_seq, row-major): entry
+ *   [b][j] is the pool page holding tokens [j * page_size, (j + 1) *
+ *   page_size) of request b.  Entries past ceil(seq_lens[b] / page_size) are
+ *   not read.
+ * seq_lens (DEVICE int32, B): tokens in each request's cache, 1 <=
+ *   seq_lens[b] <= max_seq_len, and >= Nq when causal.  Pool slots past a
+ *   request's length may hold anything (NaN included): they are not used.
+ * page_size: a power of two from 8 to 256.  max_pages_per_seq * page_size
+ *   must cover max_seq_len; num_pages * Hkv must stay below 2^31 - 1.
+ * workspace (DEVICE, 16-byte aligned, required): at least
+ *   attn_fwd_paged_workspace_bytes(...) bytes, not used by an overlapping
+ *   call.
+ * The host checks everything it can see; a page index outside [0,
+ * num_pages) or a length out of range is found by the kernel, which reads
+ * zeros for that page (or clamps the length), finishes the call and records
+ * ATTN_ERR_DEVICE_ARG for attn_device_status().  Enqueued on `stream`;
+ * nothing is allocated; the call does not synchronise. */
+attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_pages, const int *block_table,
+                             const int *seq_lens, void *O, float *LSE, int B, int Hq, int Hkv, int Nq,
+                             int max_seq_len, int d, int page_size, int num_pages, int max_pages_per_seq,
+                             int causal, int window, float sm_scale, attn_dtype_t dtype, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes attn_fwd_paged wants for these sizes on the current device
+ * (the split-KV scratch for max_seq_len keys); 0 when the sizes are invalid
+ * or the query group is too large for the split-KV kernel. */
+size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
+
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.
@@ -163,8 +210,10 @@ attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *
 size_t attn_fwd_host_staging_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_lse);
 
 /* Synchronises `stream`, then reads and clears the current device's kernel
- * status word: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up a wait since
- * the last call.  Returns ATTN_ERR_CUDA if the synchronisation fails. */
+ * status word: ATTN_OK; ATTN_ERR_TIMEOUT if a kernel gave up a wait since the
+ * last call; ATTN_ERR_DEVICE_ARG if a kernel found a device-side argument out
+ * of range (the first such event is kept).  Returns ATTN_ERR_CUDA if the
+ * synchronisation fails. */
 attn_status_t attn_device_status(cudaStream_t stream);
 
 /* Test hook: sets the bound, in nanoseconds, on every internal kernel wait of

@@ -87,3 +87,34 @@ def test_sizes(attn):
     assert attn.attn_fwd_host_staging_bytes(1, 2, 2, 64, 64, 64, 1) == 4 * q + 512
     assert attn.attn_fwd_host_staging_bytes(0, 2, 2, 64, 64, 64, 1) == 0
     assert attn.attn_fwd_workspace_bytes(1, 2, 3, 1, 64, 64) == 0  # Hq % Hkv
+
+
+@pytest.mark.parametrize("change", [
+    dict(table=None),                  # no page table
+    dict(lens=FAKE + 2),               # misaligned lengths
+    dict(page_size=12),                # not a power of two
+    dict(page_size=4),                 # below 8
+    dict(page_size=512),               # above 256
+    dict(num_pages=0),
+    dict(max_pages=3),                 # 3 pages of 16 cannot cover 64 tokens
+    dict(num_pages=1 << 30, Hkv=2),    # pool slabs past 32-bit copy coordinates
+    dict(window=8, causal=0),          # window needs causal
+    dict(Nq=65),                       # causal with more queries than keys
+    dict(Hq=3),                        # Hq % Hkv
+])
+def test_paged_host_validation(attn, change):
+    """attn_fwd_paged rejects bad arguments on the host, before touching the
+    device (the pointers are never dereferenced)."""
+    a = dict(table=FAKE, lens=FAKE, B=2, Hq=8, Hkv=2, Nq=1, max_len=64, d=128, page_size=16, num_pages=8,
+             max_pages=4, causal=1, window=0)
+    a.update(change)
+    st = attn.attn_fwd_paged(FAKE, FAKE, FAKE, a["table"], a["lens"], FAKE, None, a["B"], a["Hq"], a["Hkv"], a["Nq"],
+                             a["max_len"], a["d"], a["page_size"], a["num_pages"], a["max_pages"], a["causal"],
+                             a["window"], 0.1, 1, FAKE, 1 << 20, None)
+    assert st == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_paged_status_string(attn):
+    assert "page index" in attn.attn_status_string(attn.ATTN_ERR_DEVICE_ARG)
+    assert attn.attn_fwd_paged_workspace_bytes(1, 3, 2, 1, 64, 128) == 0  # Hq % Hkv
+    assert attn.attn_fwd_paged_workspace_bytes(1, 2, 2, 1, 64, 96) == 0   # head dim

@@ -21,6 +21,7 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_SCRATCH_LIMIT = 5
+ATTN_ERR_DEVICE_ARG = 6
 
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
@@ -33,7 +34,8 @@ ATTN_PATH_SPLIT_KV_FUSED = 4
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
-            "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits"]
+            "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
+            "attn_fwd_paged_workspace_bytes"]
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_decode_noalloc.restype = ci
         L.attn_fwd_path.argtypes = [ci, ci, ci, ci, ci, ci, ci]
         L.attn_fwd_path.restype = ci
+        L.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [ci] * 11 + [cf, ci, vp, sz, vp]
+        L.attn_fwd_paged.restype = ci
+        L.attn_fwd_paged_workspace_bytes.argtypes = [ci] * 6
+        L.attn_fwd_paged_workspace_bytes.restype = sz
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_fwd_prefill_visits.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ip, ip, ci]
         L.attn_fwd_prefill_visits.restype = ci
@@ -122,6 +128,18 @@ def attn_fwd_prefill_visits(B, Hq, Hkv, Nq, Nk, d, causal, window, with_workspac
     if got != n:
         raise RuntimeError("attn_fwd_prefill_visits: visit count changed between calls")
     return tuple(info), visits[:n]
+
+
+def attn_fwd_paged(Q, K_pages, V_pages, block_table, seq_lens, O, LSE, B, Hq, Hkv, Nq, max_seq_len, d, page_size,
+                   num_pages, max_pages_per_seq, causal, window, sm_scale, dtype, workspace, workspace_bytes,
+                   stream) -> int:
+    return lib().attn_fwd_paged(Q, K_pages, V_pages, block_table, seq_lens, O, LSE, B, Hq, Hkv, Nq, max_seq_len, d,
+                                page_size, num_pages, max_pages_per_seq, int(causal), int(window), float(sm_scale),
+                                int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d) -> int:
+    return int(lib().attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d))
 
 
 def attn_fwd_host(Qh, Kh, Vh, Oh, LSEh, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, dev_buf,
@@ -216,9 +234,54 @@ def flash_attn_forward(q, k, v, causal: bool = False, window: int = 0, sm_scale:
     return out, (lse if return_lse else None)
 
 
+def flash_attn_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, causal: bool = True,
+                     window: int = 0, sm_scale: float | None = None, return_lse: bool = True, out=None, lse=None,
+                     workspace=None):
+    """Attention over a paged K/V cache on CUDA tensors (see attn_fwd_paged
+    in include/attn.h).
+
+    q: (B, Hq, Nq, d); k_pages, v_pages: (num_pages, Hkv, page_size, d), same
+    dtype (fp16 or bf16); block_table: (B, max_pages) int32; seq_lens: (B,)
+    int32, all on q's device.  Row i of request b sits at position
+    seq_lens[b] - Nq + i.  ``workspace`` (a CUDA byte tensor of at least
+    ``attn_fwd_paged_workspace_bytes`` bytes) is allocated when not given.
+    Returns ``(O, LSE)``.  Runs on the current stream."""
+    torch = _torch()
+    ts = (q, k_pages, v_pages, block_table, seq_lens)
+    if not all(t.is_cuda for t in ts):
+        raise ValueError("flash_attn_paged needs CUDA tensors (no CPU path)")
+    if not (q.dtype == k_pages.dtype == v_pages.dtype):
+        raise TypeError("q and the page pools must share a dtype")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    if q.dim() != 4 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape or block_table.dim() != 2:
+        raise ValueError("q must be (B,Hq,Nq,d), pools (num_pages,Hkv,page_size,d), block_table (B,max_pages)")
+    q, k_pages, v_pages = q.contiguous(), k_pages.contiguous(), v_pages.contiguous()
+    block_table, seq_lens = block_table.contiguous(), seq_lens.contiguous()
+    B, Hq, Nq, d = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if k_pages.shape[3] != d or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("pools, table or lengths do not match q")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    if workspace is None:
+        need = attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = attn_fwd_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(),
+                        seq_lens.data_ptr(), out.data_ptr(), lse.data_ptr() if return_lse else None, B, Hq, Hkv, Nq,
+                        max_seq_len, d, page_size, num_pages, block_table.shape[1], causal, window, scale,
+                        _dtype_code(q), workspace.data_ptr(), workspace.numel(), _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_paged")
+    return out, (lse if return_lse else None)
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and read/clear the kernel status word."""
     return attn_device_status(_stream_handle(device))
 
 
-__all__ = EXPORTED + ["flash_attn_forward", "device_status", "lib", "AttnError"]
+__all__ = EXPORTED + ["flash_attn_forward", "flash_attn_paged", "device_status", "lib", "AttnError"]

@@ -66,6 +66,23 @@ def shape_bytes(s, with_lse: bool = True) -> int:
     return compulsory_bytes(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, 2, with_lse)
 
 
+def paged_flops(s, lens) -> float:
+    """Exact FLOPs of a paged-cache call (ai.PagedShape s, per-request key
+    counts lens): each request's live pairs at its own length."""
+    return 4.0 * s.Hq * s.d * sum(live_pairs_per_head(s.Nq, int(n), s.causal, s.window) for n in lens)
+
+
+def paged_bytes(s, lens, with_lse: bool = True) -> int:
+    """Compulsory traffic of a paged-cache call: Q and O once, each request's
+    K and V tokens once (its length, not the pool), its page-table entries
+    and its length (4 bytes each), and the LSE."""
+    b = 2 * s.d * (2 * s.B * s.Hq * s.Nq + 2 * s.Hkv * sum(int(n) for n in lens))
+    b += 4 * sum(-(-int(n) // s.page_size) for n in lens) + 4 * s.B
+    if with_lse:
+        b += 4 * s.B * s.Hq * s.Nq
+    return b
+
+
 # Page formulas (used to pin the accounting against the pages' printed numbers).
 def naive_score_traffic_bytes(N: int) -> int:
     """fp32 S written, read, written, read: 16 N^2 bytes (motivation page)."""

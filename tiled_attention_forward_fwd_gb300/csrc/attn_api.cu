@@ -323,12 +323,17 @@ static int decode_ctas_per_sm_t() {
   static int cache[64];
   static std::once_flag once[64];
   std::call_once(once[dev], [&] {
-    for (auto k : {attn_decode_kernel<D, true, RB>, attn_decode_kernel<D, false, RB>})
+    for (auto k : {attn_decode_kernel<D, true, RB, false>, attn_decode_kernel<D, false, RB, false>,
+                   attn_decode_kernel<D, true, RB, true>, attn_decode_kernel<D, false, RB, true>})
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<D, true, RB>, kDecThreads,
+    // flat and paged kernels: the smaller residency (the plan sizes one wave)
+    int n = 0, n_paged = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<D, true, RB, false>, kDecThreads,
+                                                      Cfg::kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n_paged, attn_decode_kernel<D, true, RB, true>, kDecThreads,
                                                       Cfg::kSmemBytes) != cudaSuccess)
       n = 0;
+    n = std::min(n, n_paged);
     cache[dev] = n;
   });
   return cache[dev];
@@ -384,15 +389,37 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
 }
 
 
+// A paged K/V cache: the page pool and, per request, its page table and length.
+struct PagedKV {
+  const int *block_table;
+  const int *seq_lens;
+  int page_size, num_pages, max_pages;
+};
+
 template <int D, bool BF16>
 static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                      const Shape &s, const DecPlan &pl, float *ws, int *status,
-                                     cudaStream_t stream) {
+                                     const PagedKV *pg, cudaStream_t stream) {
   DecParams p;
   std::memset(&p, 0, sizeof(p));
   const long long zk = static_cast<long long>(s.B) * s.Hkv;
-  if (!make_map(&p.tmK, K, D, s.Nk, zk, BF16, kDecKeys) || !make_map(&p.tmV, V, D, s.Nk, zk, BF16, kDecKeys))
-    return ATTN_ERR_CUDA;
+  if (pg == nullptr) {
+    if (!make_map(&p.tmK, K, D, s.Nk, zk, BF16, kDecKeys) || !make_map(&p.tmV, V, D, s.Nk, zk, BF16, kDecKeys))
+      return ATTN_ERR_CUDA;
+  } else {
+    const long long slabs = static_cast<long long>(pg->num_pages) * s.Hkv;
+    const int box = std::min(pg->page_size, kDecKeys);
+    if (!make_map(&p.tmK, K, D, pg->page_size, slabs, BF16, box) ||
+        !make_map(&p.tmV, V, D, pg->page_size, slabs, BF16, box))
+      return ATTN_ERR_CUDA;
+    p.block_table = pg->block_table;
+    p.seq_lens = pg->seq_lens;
+    int shift = 0;
+    while ((1 << shift) < pg->page_size) ++shift;
+    p.page_shift = shift;
+    p.max_pages = pg->max_pages;
+    p.num_pages = pg->num_pages;
+  }
   p.Q = Q;
   p.ws = ws;
   p.ws_lse = ws + static_cast<size_t>(s.B) * s.Hq * s.Nq * pl.nchunks * D;
@@ -426,9 +453,14 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   // (the plan already set the shared-memory attribute of both kernels)
   if (decode_ctas_per_sm(D, p.R <= 16 ? 1 : 2) <= 0) return ATTN_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(zk));
-  const cudaError_t le =
-      (p.R <= 16) ? launch_pdl(attn_decode_kernel<D, BF16, 1>, grid, dim3(kDecThreads), DecCfg<D, 1>::kSmemBytes, stream, p)
-                  : launch_pdl(attn_decode_kernel<D, BF16, 2>, grid, dim3(kDecThreads), DecCfg<D, 2>::kSmemBytes, stream, p);
+  const dim3 block(kDecThreads);
+  cudaError_t le;
+  if (pg == nullptr)
+    le = (p.R <= 16) ? launch_pdl(attn_decode_kernel<D, BF16, 1, false>, grid, block, DecCfg<D, 1>::kSmemBytes, stream, p)
+                     : launch_pdl(attn_decode_kernel<D, BF16, 2, false>, grid, block, DecCfg<D, 2>::kSmemBytes, stream, p);
+  else
+    le = (p.R <= 16) ? launch_pdl(attn_decode_kernel<D, BF16, 1, true>, grid, block, DecCfg<D, 1>::kSmemBytes, stream, p)
+                     : launch_pdl(attn_decode_kernel<D, BF16, 2, true>, grid, block, DecCfg<D, 2>::kSmemBytes, stream, p);
   if (le != cudaSuccess || cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   if (pl.fused) return ATTN_OK;
   // The merge kernel is a programmatic dependent: it may launch while the
@@ -453,15 +485,16 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
 }
 
 static attn_status_t dispatch_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
-                                     const Shape &s, const DecPlan &pl, float *ws, cudaStream_t stream) {
+                                     const Shape &s, const DecPlan &pl, float *ws, cudaStream_t stream,
+                                     const PagedKV *pg = nullptr) {
   int *status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
   const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
   if (s.d == 64)
-    return bf16 ? launch_decode_t<64, true>(Q, K, V, O, LSE, s, pl, ws, status, stream)
-                : launch_decode_t<64, false>(Q, K, V, O, LSE, s, pl, ws, status, stream);
-  return bf16 ? launch_decode_t<128, true>(Q, K, V, O, LSE, s, pl, ws, status, stream)
-              : launch_decode_t<128, false>(Q, K, V, O, LSE, s, pl, ws, status, stream);
+    return bf16 ? launch_decode_t<64, true>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream)
+                : launch_decode_t<64, false>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream);
+  return bf16 ? launch_decode_t<128, true>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream)
+              : launch_decode_t<128, false>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream);
 }
 
 // ---------------------------------------------------------------- short keys (Nk <= 128)
@@ -596,6 +629,35 @@ size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   return workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
 }
 
+attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_pages, const int *block_table,
+                             const int *seq_lens, void *O, float *LSE, int B, int Hq, int Hkv, int Nq,
+                             int max_seq_len, int d, int page_size, int num_pages, int max_pages_per_seq,
+                             int causal, int window, float sm_scale, attn_dtype_t dtype, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  Shape s{B, Hq, Hkv, Nq, max_seq_len, d, causal, window, sm_scale, dtype};
+  attn_status_t st = validate(Q, K_pages, V_pages, O, LSE, s);
+  if (st != ATTN_OK) return st;
+  if (block_table == nullptr || seq_lens == nullptr || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (page_size < 8 || page_size > 256 || (page_size & (page_size - 1)) != 0) return ATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0 || max_pages_per_seq <= 0) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(max_pages_per_seq) * page_size < max_seq_len) return ATTN_ERR_INVALID_ARG;
+  // copy coordinates are 32-bit: the pool's slabs and one past them
+  if (static_cast<long long>(num_pages) * Hkv >= 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d);
+  if (pl.bytes == 0) return ATTN_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  const PagedKV pg{block_table, seq_lens, page_size, num_pages, max_pages_per_seq};
+  return dispatch_decode(Q, K_pages, V_pages, O, LSE, s, pl, static_cast<float *>(workspace), stream, &pg);
+}
+
+size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || max_seq_len <= 0 || (d != 64 && d != 128) || Hq % Hkv) return 0;
+  return decode_plan(B, Hq, Hkv, Nq, max_seq_len, d).bytes;
+}
+
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return -1;
   Shape s{B, Hq, Hkv, Nq, Nk, d, 0, 0, 1.f, ATTN_DTYPE_FP16};
@@ -707,7 +769,7 @@ attn_status_t attn_device_status(cudaStream_t stream) {
   if (v != 0) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_ERR_TIMEOUT;
+    return v == kErrDecBadIndex ? ATTN_ERR_DEVICE_ARG : ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
 }
@@ -722,6 +784,7 @@ const char *attn_status_string(attn_status_t status) {
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
     case ATTN_ERR_SCRATCH_LIMIT: return "shape exceeds the built-in decode scratch";
+    case ATTN_ERR_DEVICE_ARG: return "a kernel found an out-of-range page index or sequence length";
   }
   return "unknown status";
 }

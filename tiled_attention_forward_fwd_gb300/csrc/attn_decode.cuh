@@ -28,6 +28,19 @@
 // launched as a programmatic dependent so that its launch overlaps kernel 1,
 // merges the chunks of every row (one CTA per row) and writes O (16-bit) and
 // LSE.
+//
+// Paged K/V (kPaged).  The motivation page's "PagedAttention es un problema
+// distinto" section: the cache is a pool of fixed-size pages (for example 16
+// tokens), each request has a table of the pages that hold its tokens in
+// order, and the attention kernel follows that table instead of reading a
+// flat K and V.  Here the pool is laid out (num_pages, Hkv, page_size, d), so
+// one (page, head) is one contiguous TMA box; a 64-key tile is 64 / page_size
+// boxes (or a 64-row part of one page), placed back to back in shared memory,
+// where they form the same 128B-swizzled tile as one 64-row box.  The
+// producer reads the next tile's page indices while the current tile's copies
+// go out.  Each request has its own length (read on the device); slots past
+// it in the last page hold whatever the pool held, so their V rows are
+// zeroed in shared memory before P V (their P is 0, but 0 x NaN is not).
 #pragma once
 
 #include <stddef.h>
@@ -43,10 +56,12 @@ constexpr int kDecMaxRows = 32;  // query rows of one group handled by one CTA
 constexpr int kDecMaxChunks = 1024;  // key chunks per group (bounds the merge kernel's shared memory)
 constexpr int kDecFusedMerge = 8192;  // rows x chunks x d of a group merged by the split kernel itself
 
-enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecWaitPartial = 0x202 };
+enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecWaitPartial = 0x202, kErrDecBadIndex = 0x203 };
 
 struct DecParams {
-  CUtensorMap tmK;  // (d, Nk, B*Hkv), box 64 x 64 x 1, 128B swizzle
+  // flat: (d, Nk, B*Hkv), box 64 x 64 x 1; paged: (d, page_size,
+  // num_pages*Hkv), box 64 x min(page_size, 64) x 1; 128B swizzle
+  CUtensorMap tmK;
   CUtensorMap tmV;
   const void *Q;    // (B, Hq, Nq, d), 16-bit
   float *ws;        // [B*Hq*Nq][nchunks][d]: normalised O of each chunk
@@ -65,6 +80,13 @@ struct DecParams {
   int kv_lo, kv_hi;  // keys any row of a group can see
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
+  // paged K/V: token t of request b sits in page block_table[b * max_pages +
+  // t / page_size], slot t % page_size; request b holds seq_lens[b] tokens
+  // (1..Nk, at least Nq when causal); kv_lo and kv_hi are not used
+  const int *block_table;
+  const int *seq_lens;
+  int page_shift;  // log2(page_size), 3..8
+  int max_pages, num_pages;
 };
 
 // Ring depth and resident CTAs per SM for (d, row blocks).  Tiles arrive
@@ -136,8 +158,8 @@ __device__ __forceinline__ void mbar_drain_dec(uint32_t bar, uint32_t parity) {
 }
 
 // Partial attention of one GQA group over one key chunk.  RB = row blocks of
-// 16 (1: up to 16 rows, 2: up to 32).
-template <int D, bool BF16, int RB>
+// 16 (1: up to 16 rows, 2: up to 32); kPaged: K and V come from a page pool.
+template <int D, bool BF16, int RB, bool kPaged>
 __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
     attn_decode_kernel(const __grid_constant__ DecParams p) {
   using C = DecCfg<D, RB>;
@@ -161,9 +183,6 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
   const int chunk = blockIdx.x;
   const int bk = blockIdx.y;  // b * Hkv + kvh
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
-  const int k0 = max(chunk * p.chunk_keys, p.kv_lo);
-  const int k1 = min((chunk + 1) * p.chunk_keys, p.kv_hi);
-  const int ntiles = (k1 > k0) ? (k1 - k0 + kDecKeys - 1) / kDecKeys : 0;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
   // Let the merge kernel launch now; it waits for this grid to finish
@@ -183,6 +202,23 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
   __syncthreads();
   pdl_wait();  // inputs may come from the previous kernel on the stream
   bool ok = true;
+  // keys of this request, and the ones this chunk takes
+  int nk = p.kv_hi, kv_lo = p.kv_lo;
+  if constexpr (kPaged) {
+    int len = __ldcg(p.seq_lens + b);
+    if (len < (p.causal ? p.Nq : 1) || len > p.Nk) {
+      if (threadIdx.x == 0) atomicCAS(p.status, 0, kErrDecBadIndex);
+      len = min(max(len, 0), p.Nk);
+    }
+    nk = len;
+    // the first key any row of the group can see, rounded down to a tile
+    // boundary so that every tile starts on a page boundary (keys below the
+    // window are masked per key)
+    kv_lo = (p.causal && p.window > 0) ? max(0, nk - p.Nq - p.window + 1) & ~(kDecKeys - 1) : 0;
+  }
+  const int k0 = max(chunk * p.chunk_keys, kv_lo);
+  const int k1 = min((chunk + 1) * p.chunk_keys, nk);
+  const int ntiles = (k1 > k0) ? (k1 - k0 + kDecKeys - 1) / kDecKeys : 0;
 
   if (warp == kDecWarps) {
     // ======================================================== TMA producer
@@ -193,18 +229,64 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       tma_prefetch_desc(&p.tmV);
     }
     __syncwarp();
+    // Paged: lane j < npg reads the pool slab (page * Hkv + kvh) of the j-th
+    // page of a tile.  A page past the request's end, or an index outside
+    // the pool (recorded as an error), becomes the first slab past the pool,
+    // which the copy reads as zeros.
+    constexpr int kMaxTilePages = kDecKeys / 8;  // page_size >= 8
+    const int pshift = kPaged ? p.page_shift : 0;
+    const int npg = (kPaged && pshift < 6) ? (kDecKeys >> pshift) : 1;
+    const int req_pages = kPaged ? ((nk + (1 << pshift) - 1) >> pshift) : 0;
+    const int past_pool = kPaged ? p.num_pages * p.Hkv : 0;
+    auto tile_page = [&](int i) { return ((k0 + i * kDecKeys) >> pshift) + lane; };
+    auto read_page = [&](int i) {
+      const int lp = tile_page(i);
+      return (lane < npg && lp < req_pages) ? __ldcg(p.block_table + static_cast<size_t>(b) * p.max_pages + lp) : 0;
+    };
+    int page_next = (kPaged && ntiles > 0) ? read_page(0) : 0;
     int kiss = 0, viss = 0;  // K / V tiles issued
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % NS, y = k0 + i * kDecKeys;
       const uint32_t kdst = sKV + s * C::kStageBytes, vdst = kdst + C::kTileBytes;
+      int slab[kMaxTilePages];
+      if constexpr (kPaged) {
+        const int page = page_next;
+        if (i + 1 < ntiles) page_next = read_page(i + 1);  // in flight during this tile's waits
+        int z = past_pool;
+        if (lane < npg && tile_page(i) < req_pages) {
+          if (page >= 0 && page < p.num_pages)
+            z = page * p.Hkv + kvh;
+          else
+            atomicCAS(p.status, 0, kErrDecBadIndex);
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxTilePages; ++j) slab[j] = __shfl_sync(0xffffffffu, z, j);
+      }
+      // one K or V tile into dst: a 64-row box per 64 columns (flat), or per
+      // page and 64 columns (paged)
+      auto load_tile = [&](uint32_t dst, const CUtensorMap *tm, uint32_t bar) {
+        if constexpr (!kPaged) {
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(dst + cc * C::kBoxBytes, tm, bar, cc * 64, y, bk);
+        } else if (pshift >= 6) {
+          const int row = y & ((1 << pshift) - 1);  // a multiple of 64
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(dst + cc * C::kBoxBytes, tm, bar, cc * 64, row, slab[0]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc)
+#pragma unroll
+            for (int j = 0; j < kMaxTilePages; ++j)
+              if (j < npg) tma_load_3d(dst + cc * C::kBoxBytes + (j << pshift) * 128, tm, bar, cc * 64, 0, slab[j]);
+        }
+      };
       if (i >= NS && !mbar_wait_warp(bKempty(s), ((i / NS) - 1) & 1, wc, kErrDecWaitKV)) {
         ok = false;
         break;
       }
       if (elect_one()) {
         mbar_arrive_expect_tx(bKfull(s), C::kTileBytes);
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(kdst + cc * C::kBoxBytes, &p.tmK, bKfull(s), cc * 64, y, bk);
+        load_tile(kdst, &p.tmK, bKfull(s));
       }
       __syncwarp();
       kiss = i + 1;
@@ -214,8 +296,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       }
       if (elect_one()) {
         mbar_arrive_expect_tx(bVfull(s), C::kTileBytes);
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(vdst + cc * C::kBoxBytes, &p.tmV, bVfull(s), cc * 64, y, bk);
+        load_tile(vdst, &p.tmV, bVfull(s));
       }
       __syncwarp();
       viss = i + 1;
@@ -255,7 +336,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       m[rb][h] = -INFINITY;
       l[rb][h] = 0.f;
       rowok[rb][h] = r < p.R;
-      pos[rb][h] = p.Nk - p.Nq + (r % p.Nq);
+      pos[rb][h] = nk - p.Nq + (r % p.Nq);
     }
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[rb][n][0] = o[rb][n][1] = o[rb][n][2] = o[rb][n][3] = 0.f;
@@ -342,6 +423,18 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
     if (!mbar_wait_warp(bVfull(s), (i / NS) & 1, wc, kErrDecWaitKV)) {
       ok = false;
       break;
+    }
+    if (kPaged && key_base + 16 > nk) {
+      // this warp's V rows past the request's end: zero them (16-byte
+      // pieces; a whole 128-byte row of a box is swizzle-free), then order
+      // these writes before the next copy into the stage
+      for (int idx = lane; idx < 16 * (D / 64) * 8; idx += 32) {
+        const int r = idx / ((D / 64) * 8), cc = (idx / 8) % (D / 64), piece = idx % 8;
+        if (key_base + r >= nk)
+          st_shared_v4(sV + cc * C::kBoxBytes + (warp * 16 + r) * 128 + piece * 16, 0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
     }
     {
       const int j = lane >> 3;
