@@ -199,8 +199,7 @@ def prepare_paged(shape, cid, layer, device):
     c["label"] = call_label(shape)
     wsb = attn.attn_fwd_paged_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.max_seq_len, shape.d)
     c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device)
-    # the split-KV plan of max_seq_len keys (the same plan as a flat call)
-    path = attn.attn_fwd_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.max_seq_len, shape.d, True)
+    path = attn.attn_fwd_paged_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.max_seq_len, shape.d)
     c["path"] = path
     c["kernel"] = "attn_decode_kernel[paged]"
     c["launches"] = 2 if path == attn.ATTN_PATH_SPLIT_KV else 1

@@ -196,6 +196,15 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
  * or the query group is too large for the split-KV kernel. */
 size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
 
+/* The path attn_fwd_paged takes for these sizes on the current device:
+ * ATTN_PATH_SPLIT_KV_FUSED (each group's last-chunk CTA merges the chunks:
+ * one launch) or ATTN_PATH_SPLIT_KV (a second, merge kernel); -1 when the
+ * sizes are invalid or the query group is too large.  The paged plan caps
+ * the keys per chunk, since request lengths are known only on the device,
+ * so it can split more finely than the flat call of max_seq_len keys.  No
+ * device work. */
+int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
+
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.

@@ -191,3 +191,18 @@ def test_workload_full_size(attn, oracle_mod, idx):
     oracle."""
     shape, cid, layer = ai.workload_calls("paged_decode")[idx]
     check(attn, oracle_mod, shape, cid, layer)
+
+
+def test_paged_plan(attn):
+    """The paged plan caps the keys per chunk (lengths are known only on the
+    device): the ragged benchmark call keeps the fused merge, the group too
+    large for the split-KV kernel has no paged path, and a full-length call
+    that already splits finely plans like the flat call."""
+    assert attn.attn_fwd_paged_path(32, 32, 8, 1, 8192, 128) == attn.ATTN_PATH_SPLIT_KV_FUSED
+    assert attn.attn_fwd_paged_path(1, 8, 1, 8, 256, 64) == -1
+    assert attn.attn_fwd_paged_path(4, 32, 8, 1, 8192, 128) == attn.attn_fwd_path(4, 32, 8, 1, 8192, 128, True)
+    assert attn.attn_fwd_paged_workspace_bytes(4, 32, 8, 1, 8192, 128) == \
+        attn.attn_fwd_workspace_bytes(4, 32, 8, 1, 8192, 128)
+    # a long-context batch: more chunks than the flat plan, so more scratch
+    assert attn.attn_fwd_paged_workspace_bytes(32, 32, 8, 1, 8192, 128) > \
+        attn.attn_fwd_workspace_bytes(32, 32, 8, 1, 8192, 128)

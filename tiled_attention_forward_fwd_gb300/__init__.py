@@ -35,7 +35,7 @@ ATTN_PATH_SPLIT_KV_FUSED = 4
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
-            "attn_fwd_paged_workspace_bytes"]
+            "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_paged.restype = ci
         L.attn_fwd_paged_workspace_bytes.argtypes = [ci] * 6
         L.attn_fwd_paged_workspace_bytes.restype = sz
+        L.attn_fwd_paged_path.argtypes = [ci] * 6
+        L.attn_fwd_paged_path.restype = ci
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_fwd_prefill_visits.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ip, ip, ci]
         L.attn_fwd_prefill_visits.restype = ci
@@ -140,6 +142,10 @@ def attn_fwd_paged(Q, K_pages, V_pages, block_table, seq_lens, O, LSE, B, Hq, Hk
 
 def attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d) -> int:
     return int(lib().attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d))
+
+
+def attn_fwd_paged_path(B, Hq, Hkv, Nq, max_seq_len, d) -> int:
+    return int(lib().attn_fwd_paged_path(B, Hq, Hkv, Nq, max_seq_len, d))
 
 
 def attn_fwd_host(Qh, Kh, Vh, Oh, LSEh, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, dev_buf,

@@ -344,11 +344,20 @@ static int decode_ctas_per_sm(int d, int rb) {
   return rb == 1 ? decode_ctas_per_sm_t<128, 1>() : decode_ctas_per_sm_t<128, 2>();
 }
 
+// Paged calls: each request's length is known only on the device, and the
+// lengths of a batch may differ widely.  A plan sized for max_seq_len keys
+// in every request can leave the longest requests to single CTAs that
+// stream on long after the others have finished, so their chunks hold at
+// most this many K/V tiles (chunks past a short request's end are empty and
+// end at once).
+constexpr int kPagedMaxChunkTiles = 32;
+
 // The split-KV path serves shapes whose GQA group holds at most 32 query rows
 // (decode: Nq = 1 with up to 32 query heads per K/V head).  The number of
 // chunks per group minimises (waves of CTAs) x (K/V tiles per CTA + a fixed
 // cost of about two tiles per CTA): usually one full wave of resident CTAs.
-static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+// `ragged` (paged calls) also caps the tiles per chunk.
+static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool ragged = false) {
   DecPlan pl;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return pl;
   const long long R = static_cast<long long>(Hq / Hkv) * Nq;
@@ -369,6 +378,10 @@ static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
       best_cost = cost;
       best_n = n;
     }
+  }
+  if (ragged) {
+    const long long cap_n = (tiles + kPagedMaxChunkTiles - 1) / kPagedMaxChunkTiles;
+    best_n = std::max(best_n, std::min<long long>(cap_n, kDecMaxChunks));
   }
   int chunk_keys = static_cast<int>((Nk + best_n - 1) / best_n);
   chunk_keys = ((chunk_keys + kDecKeys - 1) / kDecKeys) * kDecKeys;
@@ -646,16 +659,23 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
   // copy coordinates are 32-bit: the pool's slabs and one past them
   if (static_cast<long long>(num_pages) * Hkv >= 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
-  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d);
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
   if (pl.bytes == 0) return ATTN_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   const PagedKV pg{block_table, seq_lens, page_size, num_pages, max_pages_per_seq};
   return dispatch_decode(Q, K_pages, V_pages, O, LSE, s, pl, static_cast<float *>(workspace), stream, &pg);
 }
 
+int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || max_seq_len <= 0 || (d != 64 && d != 128) || Hq % Hkv) return -1;
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
+  if (pl.bytes == 0) return -1;
+  return pl.fused ? ATTN_PATH_SPLIT_KV_FUSED : ATTN_PATH_SPLIT_KV;
+}
+
 size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || max_seq_len <= 0 || (d != 64 && d != 128) || Hq % Hkv) return 0;
-  return decode_plan(B, Hq, Hkv, Nq, max_seq_len, d).bytes;
+  return decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true).bytes;
 }
 
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace) {
