@@ -46,7 +46,15 @@ WORKLOAD_TEXT = {
     "paged_decode": "decode on a paged cache (16-token pages, shuffled pool), Hq=32, Hkv=8, Nq=1, d=128, bf16: "
                     "B=4 at 8192 tokens; B=32 at drawn lengths 512..8192",
 }
-KERNEL_SOURCES = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_decode.cuh", "attn_short.cuh", "sm103_ptx.cuh", "fastdiv.h"]
+# Device sources of each kernel family: a committed DRAM-traffic figure
+# (profiles/traffic.json) counts only while they hash to the value recorded
+# with it.  (Host launch code is not part of the key: an entry is re-taken
+# whenever a path's launch configuration changes.)
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["attn_fwd_sm103.cuh", "sm103_ptx.cuh", "fastdiv.h"],
+    "attn_decode_kernel": ["attn_decode.cuh", "sm103_ptx.cuh"],
+    "attn_short_kernel": ["attn_short.cuh", "sm103_ptx.cuh"],
+}
 
 
 def parse_args():
@@ -152,24 +160,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the device sources of a kernel family ("attn_fwd_kernel", ...)."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel.split("[")[0]]:
         with open(os.path.join(ROOT, "tiled_attention_forward_fwd_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, call_label: str):
-    """DRAM bytes per launch from a committed ncu summary, only if the kernel
-    sources are unchanged since it was taken (else None)."""
+def profiled_traffic(workload: str, call_label: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, only if the
+    kernel's sources are unchanged since it was taken (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(call_label)
-    if not e or e.get("kernel_src_sha") != kernel_source_hash():
+    if not e or e.get("kernel_src_sha") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -561,7 +570,7 @@ def main():
         achieved = dc["bytes"] / (avg[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
-    roof["traffic"] = profiled_traffic(args.workload, dc["label"])
+    roof["traffic"] = profiled_traffic(args.workload, dc["label"], dc["kernel"])
     roof["kernel"] = f"{dc['kernel']}<{s.d},{'bf16' if s.dtype == 'bf16' else 'fp16'}> {dc['label']}"
     roof["algorithmic"] = {"flops": dc["flops"], "bytes": dc["bytes"]}
     roof["peak_source"] = f"{peaks_src} (burst bf16 dense; fp16 same rate)" if roof["bound"] == "tensor" \
