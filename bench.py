@@ -98,6 +98,12 @@ def dist_max(ws, x: float, device) -> float:
     return float(t.item())
 
 
+def job_value(ws: int, flops_step: float, steps: int, max_total_ms: float) -> float:
+    """Whole-job TFLOP/s of ws replicas (weak scaling: every rank runs the
+    same step), each timed over `steps` steps, against the slowest rank."""
+    return ws * flops_step * steps / (max_total_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- peaks, clocks, profiles
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -551,7 +557,7 @@ def main():
 
     total_ms = dist_max(ws, float(sum(step_ms)), device)
     flops_step = sum(c["flops"] for c in calls)
-    value = ws * flops_step * steps / (total_ms * 1e-3) / 1e12
+    value = job_value(ws, flops_step, steps, total_ms)
     ms_per_step = total_ms / steps
 
     # dominant kernel: the call with the largest share of device time
