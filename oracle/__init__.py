@@ -61,6 +61,9 @@ def _load():
             lib.oracle_attn_paged.argtypes = [dp, dp, dp, i32p, i32p, dp, dp, ci, ci, ci, ci, ci, ci, ci,
                                               ci, ci, ci, ctypes.c_double, ci]
             lib.oracle_attn_paged.restype = ci
+            lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci, ci,
+                                            ctypes.c_double]
+            lib.oracle_attn_bwd.restype = ci
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -151,3 +154,21 @@ def attention_paged(q, k_pool, v_pool, block_table, seq_lens, causal: bool = Fal
     if rc != 0:
         raise ValueError(f"oracle_attn_paged failed with code {rc}")
     return o, lse
+
+
+def attention_bwd(q, k, v, do, causal: bool = False, window: int = 0, sm_scale: float | None = None):
+    """fp64 gradients of the forward definition for upstream gradient ``do``:
+    returns ``(dQ, dK, dV)`` as float64 numpy arrays shaped like q, k, v (dK
+    and dV summed over each kv head's query heads)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if do.shape != q.shape or v.shape != k.shape:
+        raise ValueError("attention_bwd: inconsistent shapes")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / float(np.sqrt(d))
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv,
+                                 Nq, Nk, d, int(bool(causal)), int(window), scale)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd failed with code {rc}")
+    return dq, dk, dv

@@ -277,3 +277,98 @@ int oracle_attn_paged(const double *Q, const double *Kpool, const double *Vpool,
   }
   return failed ? ORACLE_ENOMEM : ORACLE_OK;
 }
+
+/* Gradients of the forward definition above (the pages keep the LSE "for
+ * the backward pass" and leave the backward itself for later; what it
+ * computes is fixed by the forward: the chain rule through steps 4-6).  For
+ * a loss with dO = dL/dO, per query row i of head h (kv head kvh), with the
+ * row's normalised weights P_ij (0 for masked keys) from steps 4-5:
+ *   dV[kvh,j]  += P_ij dO_i                       (step 6 is linear in V)
+ *   dP_ij       = dO_i . V[kvh,j]
+ *   dS_ij       = P_ij (dP_ij - sum_k P_ik dP_ik)  (softmax Jacobian)
+ *   dQ_i        = sm_scale sum_j dS_ij K[kvh,j]    (step 4)
+ *   dK[kvh,j]  += sm_scale dS_ij Q_i
+ * dK and dV of a kv head sum over the query heads of its group.  Q, dO, dQ:
+ * B x Hq x Nq x d; K, V, dK, dV: B x Hkv x Nk x d.  Every row must have a
+ * live key (the forward's R4 reading); rows without one return
+ * ORACLE_EINVAL.  Serial over heads (dK/dV accumulate across a group). */
+int oracle_attn_bwd(const double *Q, const double *K, const double *V,
+                    const double *dO, double *dQ, double *dK, double *dV,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                    int window, double sm_scale) {
+  int rc = check_args(B, Hq, Hkv, Nq, Nk, d, sm_scale);
+  if (rc) return rc;
+  if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return ORACLE_EINVAL;
+  const int g = Hq / Hkv;
+  double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
+  double *dp = (double *)malloc(sizeof(double) * (size_t)Nk);
+  if (!p || !dp) {
+    free(p);
+    free(dp);
+    return ORACLE_ENOMEM;
+  }
+  for (long x = 0; x < (long)B * Hkv * Nk * d; ++x) dK[x] = dV[x] = 0.0;
+  rc = ORACLE_OK;
+  for (long b = 0; b < B && rc == ORACLE_OK; ++b) {
+    for (long h = 0; h < Hq && rc == ORACLE_OK; ++h) {
+      const long kvh = h / g;
+      const double *Kh = K + ((b * Hkv + kvh) * (long)Nk) * d;
+      const double *Vh = V + ((b * Hkv + kvh) * (long)Nk) * d;
+      double *dKh = dK + ((b * Hkv + kvh) * (long)Nk) * d;
+      double *dVh = dV + ((b * Hkv + kvh) * (long)Nk) * d;
+      for (long i = 0; i < Nq; ++i) {
+        const long r = (b * Hq + h) * (long)Nq + i;
+        const double *q = Q + r * d, *go = dO + r * d;
+        double *gq = dQ + r * d;
+        const long pos = Nk - Nq + i;
+        /* steps 4-5: the row's weights */
+        double M = -INFINITY;
+        for (long j = 0; j < Nk; ++j) {
+          if (!key_is_live(pos, j, causal, window)) {
+            p[j] = -INFINITY;
+            continue;
+          }
+          double dot = 0.0;
+          for (long c = 0; c < d; ++c) dot += q[c] * Kh[j * d + c];
+          p[j] = sm_scale * dot;
+          if (p[j] > M) M = p[j];
+        }
+        if (M == -INFINITY) {
+          rc = ORACLE_EINVAL;
+          break;
+        }
+        double l = 0.0;
+        for (long j = 0; j < Nk; ++j) {
+          p[j] = (p[j] == -INFINITY) ? 0.0 : exp(p[j] - M);
+          l += p[j];
+        }
+        for (long j = 0; j < Nk; ++j) p[j] /= l;
+        /* dP and its P-weighted row sum */
+        double Dsum = 0.0;
+        for (long j = 0; j < Nk; ++j) {
+          if (p[j] == 0.0) {
+            dp[j] = 0.0;
+            continue;
+          }
+          double dot = 0.0;
+          for (long c = 0; c < d; ++c) dot += go[c] * Vh[j * d + c];
+          dp[j] = dot;
+          Dsum += p[j] * dot;
+        }
+        for (long c = 0; c < d; ++c) gq[c] = 0.0;
+        for (long j = 0; j < Nk; ++j) {
+          if (p[j] == 0.0) continue;
+          const double ds = p[j] * (dp[j] - Dsum);
+          for (long c = 0; c < d; ++c) {
+            dVh[j * d + c] += p[j] * go[c];
+            gq[c] += sm_scale * ds * Kh[j * d + c];
+            dKh[j * d + c] += sm_scale * ds * q[c];
+          }
+        }
+      }
+    }
+  }
+  free(p);
+  free(dp);
+  return rc;
+}
