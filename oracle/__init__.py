@@ -172,3 +172,25 @@ def attention_bwd(q, k, v, do, causal: bool = False, window: int = 0, sm_scale: 
     if rc != 0:
         raise ValueError(f"oracle_attn_bwd failed with code {rc}")
     return dq, dk, dv
+
+
+def attention_mla(q, c, w_k_up, w_v_up, causal: bool = False, window: int = 0, sm_scale: float | None = None):
+    """fp64 attention over a latent K/V cache (Multi-Head Latent Attention,
+    cruxr.ai "Optimizaciones de Atencion", "Multi-Head Latent Attention
+    (MLA)"): each token caches one vector c_t of d_c values, and keys and
+    values are rebuilt per head by the up-projections
+    K = c W_K^up, V = c W_V^up (W: d_c x (n_h * d_h)).
+
+    q: (B, n_h, Nq, d_h); c: (B, Nk, d_c); w_k_up, w_v_up: (d_c, n_h * d_h).
+    The keys and values of every head are decompressed explicitly (one matrix
+    product each), then the plain definition runs as attention with n_h kv
+    heads.  Returns ``(O, LSE)``, O (B, n_h, Nq, d_h)."""
+    q, c, wk, wv = _f64(q), _f64(c), _f64(w_k_up), _f64(w_v_up)
+    B, n_h, Nq, d_h = q.shape
+    Nk, d_c = c.shape[1], c.shape[2]
+    if c.shape[0] != B or wk.shape != (d_c, n_h * d_h) or wv.shape != wk.shape:
+        raise ValueError("attention_mla: inconsistent shapes")
+    k = (c @ wk).reshape(B, Nk, n_h, d_h).transpose(0, 2, 1, 3)
+    v = (c @ wv).reshape(B, Nk, n_h, d_h).transpose(0, 2, 1, 3)
+    return attention(q, k, v, causal=causal, window=window,
+                     sm_scale=sm_scale if sm_scale is not None else 1.0 / float(np.sqrt(d_h)))
