@@ -220,6 +220,17 @@ def make_paged(shape: PagedShape, config_id: int = 0, layer: int = 0, poison: bo
     return q, k, v, torch.from_numpy(table), torch.from_numpy(lens.astype(np.int32))
 
 
+def quantize_int8(x: torch.Tensor):
+    """Symmetric per-tensor INT8 codes of x: scale = max|x| / 127 (fp32),
+    codes = round-half-even(x / scale) as int8.  Returns (codes, scale)."""
+    xf = x.to(torch.float32)
+    amax = float(xf.abs().max())
+    scale = amax / 127.0 if amax > 0 else 1.0
+    scale = float(np.float32(scale))
+    codes = torch.round(xf / scale).clamp_(-127, 127).to(torch.int8)
+    return codes, scale
+
+
 def sha256_of(t: torch.Tensor) -> str:
     t = t.contiguous()
     if t.dtype == torch.bfloat16:

@@ -194,3 +194,20 @@ def attention_mla(q, c, w_k_up, w_v_up, causal: bool = False, window: int = 0, s
     v = (c @ wv).reshape(B, Nk, n_h, d_h).transpose(0, 2, 1, 3)
     return attention(q, k, v, causal=causal, window=window,
                      sm_scale=sm_scale if sm_scale is not None else 1.0 / float(np.sqrt(d_h)))
+
+
+def attention_kv_int8(q, k_codes, v_codes, k_scale: float, v_scale: float, causal: bool = False, window: int = 0,
+                      sm_scale: float | None = None):
+    """fp64 attention over an INT8-quantised K/V cache (cruxr.ai
+    "Optimizaciones de Atencion", "Elegir optimizaciones de atencion": INT8
+    quantisation of the KV cache composes with the rest).  Symmetric codes
+    with one fp32 scale per tensor: K = k_scale * k_codes, V = v_scale *
+    v_codes (codes in [-127, 127]).  The cache is dequantised exactly in
+    fp64, then the plain definition runs.  Returns ``(O, LSE)``."""
+    kc, vc = _f64(k_codes), _f64(v_codes)
+    if kc.shape != vc.shape or np.abs(kc).max(initial=0) > 127 or np.abs(vc).max(initial=0) > 127 or \
+            not np.array_equal(kc, np.round(kc)) or not np.array_equal(vc, np.round(vc)):
+        raise ValueError("attention_kv_int8: codes must be integers in [-127, 127] of equal shapes")
+    if not (k_scale > 0 and v_scale > 0 and np.isfinite(k_scale) and np.isfinite(v_scale)):
+        raise ValueError("attention_kv_int8: scales must be positive and finite")
+    return attention(q, float(k_scale) * kc, float(v_scale) * vc, causal=causal, window=window, sm_scale=sm_scale)
