@@ -8,9 +8,12 @@ fallback.
 The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows):
 the materialised score row, batch softmax and weighted sum of V, exactly as the
 lab 02 page's PyTorch reference ("Bloque C") and the standard-attention half of
-the cruxr.ai worked example define attention.  This module only builds the
-library with gcc and marshals arrays; it adds no arithmetic of its own beyond
-the exact upcast of the stored fp16/bf16 inputs to float64.
+the cruxr.ai worked example define attention; the gather through a page table;
+and the gradients of that definition.  This module builds the library with gcc
+and marshals arrays.  Its own arithmetic is limited to the exact upcast of the
+stored fp16/bf16 inputs to float64, the latent cache's up-projections (one
+numpy matrix product each, ``attention_mla``) and the INT8 cache's dequantising
+multiply (``attention_kv_int8``), each followed by the C definition.
 """
 from __future__ import annotations
 
