@@ -118,3 +118,24 @@ def test_paged_status_string(attn):
     assert "page index" in attn.attn_status_string(attn.ATTN_ERR_DEVICE_ARG)
     assert attn.attn_fwd_paged_workspace_bytes(1, 3, 2, 1, 64, 128) == 0  # Hq % Hkv
     assert attn.attn_fwd_paged_workspace_bytes(1, 2, 2, 1, 64, 96) == 0   # head dim
+
+
+def test_maximum_sizes_rejected(attn):
+    """Work items are counted in 32 bits: a call with more than 2^31 - 1
+    query tiles (B * Hq * ceil(Nq / 128)) is rejected on the host, before any
+    launch (the pointers are never used, on any machine)."""
+    too_many = attn.attn_fwd(FAKE, FAKE, FAKE, FAKE, None, 65536, 256, 256, 1 << 20, 64, 1, 0, 0.125, 0, None)
+    assert too_many == attn.ATTN_ERR_INVALID_ARG
+    B, H, N = 16384, 1024, 16384  # 16384 * 1024 * 128 tiles = 2^31, one past the limit
+    assert attn.attn_fwd(FAKE, FAKE, FAKE, FAKE, None, B, H, H, N, 64, 0, 0, 0.125, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    # the schedule query refuses item lists past 32 bits as well
+    assert attn.attn_fwd_prefill_visits(65536, 256, 256, 1 << 20, 1 << 20, 64, 1, 0, 0, 152) is None
+
+
+def test_size_queries_do_not_overflow(attn):
+    """Byte counts are 64-bit: a 2^31-element tensor's staging size is exact."""
+    B, H, N, d = 4, 32, 131072, 128  # Q is 2^31 elements
+    q_bytes = B * H * N * d * 2
+    got = attn.attn_fwd_host_staging_bytes(B, H, H, N, N, d, 1)
+    lse = B * H * N * 4
+    assert got >= 4 * q_bytes + lse and got < 4 * q_bytes + lse + 5 * 256 + (1 << 30)
