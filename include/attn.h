@@ -132,6 +132,19 @@ size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * path.  No device work. */
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace);
 
+/* The split-KV plan for these sizes on a device of `sms` SMs holding
+ * `ctas_per_sm` split CTAs each (the occupancy of the split kernel), without
+ * device work (cruxr.ai "FlashDecoding": the keys are cut into chunks that
+ * are processed in parallel, then merged).  paged != 0 gives attn_fwd_paged's
+ * plan (at most 2048 keys a chunk, max_seq_len = Nk).  info (HOST, 5
+ * values, written): chunks per GQA group, keys per chunk (a multiple of 64;
+ * the last chunk may be shorter), 1 when each group's last-chunk CTA merges
+ * (one launch) else 0, byte offset of the merge flags in the workspace, and
+ * the workspace bytes.  Returns 0, or -1 when the shape does not take the
+ * split-KV path ((Hq / Hkv) * Nq > 32, B * Hkv > 65535, bad sizes). */
+int attn_fwd_decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int paged, int sms, int ctas_per_sm,
+                         long long *info);
+
 /* The prefill kernel's schedule for these sizes, without device work: what
  * attn_fwd_ex would launch on a device of `sms` SMs (FlashAttention-2,
  * "Parallelism": query tiles of 128 rows as independent units, each walking

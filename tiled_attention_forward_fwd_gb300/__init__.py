@@ -35,7 +35,8 @@ ATTN_PATH_SPLIT_KV_FUSED = 4
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_staging_bytes",
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
-            "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path"]
+            "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
+            "attn_fwd_decode_plan"]
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_paged_workspace_bytes.restype = sz
         L.attn_fwd_paged_path.argtypes = [ci] * 6
         L.attn_fwd_paged_path.restype = ci
+        L.attn_fwd_decode_plan.argtypes = [ci] * 9 + [ctypes.POINTER(ctypes.c_longlong)]
+        L.attn_fwd_decode_plan.restype = ci
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_fwd_prefill_visits.argtypes = [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ip, ip, ci]
         L.attn_fwd_prefill_visits.restype = ci
@@ -111,6 +114,15 @@ def attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
 
 def attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, with_workspace) -> int:
     return int(lib().attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, 1 if with_workspace else 0))
+
+
+def attn_fwd_decode_plan(B, Hq, Hkv, Nq, Nk, d, paged, sms, ctas_per_sm):
+    """The split-KV plan without device work: dict(nchunks, chunk_keys,
+    fused, flag_off, bytes), or None when the shape takes no split-KV path."""
+    info = (ctypes.c_longlong * 5)()
+    if lib().attn_fwd_decode_plan(B, Hq, Hkv, Nq, Nk, d, 1 if paged else 0, sms, ctas_per_sm, info) != 0:
+        return None
+    return dict(zip(("nchunks", "chunk_keys", "fused", "flag_off", "bytes"), (int(x) for x in info)))
 
 
 def attn_fwd_prefill_visits(B, Hq, Hkv, Nq, Nk, d, causal, window, with_workspace, sms):

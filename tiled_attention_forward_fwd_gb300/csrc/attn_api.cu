@@ -357,13 +357,12 @@ constexpr int kPagedMaxChunkTiles = 32;
 // chunks per group minimises (waves of CTAs) x (K/V tiles per CTA + a fixed
 // cost of about two tiles per CTA): usually one full wave of resident CTAs.
 // `ragged` (paged calls) also caps the tiles per chunk.
-static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool ragged = false) {
+// The plan for a device of `sms` SMs with `per_sm` resident split CTAs each.
+static DecPlan decode_plan_for(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool ragged, int sms, int per_sm) {
   DecPlan pl;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return pl;
   const long long R = static_cast<long long>(Hq / Hkv) * Nq;
   if (R > kDecMaxRows) return pl;
-  const int sms = device_sm_count();
-  const int per_sm = decode_ctas_per_sm(d, R <= 16 ? 1 : 2);
   if (sms <= 0 || per_sm <= 0) return pl;
   const long long units = static_cast<long long>(B) * Hkv;
   if (units > 65535) return pl;  // grid.y limit
@@ -395,6 +394,13 @@ static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool r
   pl.flag_off = (part + 15) & ~size_t(15);
   pl.bytes = pl.flag_off + static_cast<size_t>(units) * pl.nchunks * sizeof(unsigned);
   return pl;
+}
+
+static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool ragged = false) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return {};
+  const long long R = static_cast<long long>(Hq / Hkv) * Nq;
+  if (R > kDecMaxRows) return {};
+  return decode_plan_for(B, Hq, Hkv, Nq, Nk, d, ragged, device_sm_count(), decode_ctas_per_sm(d, R <= 16 ? 1 : 2));
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
@@ -686,6 +692,19 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
   if (with_workspace && dp.bytes > 0) return dp.fused ? ATTN_PATH_SPLIT_KV_FUSED : ATTN_PATH_SPLIT_KV;
   if (with_workspace && split_plan_bytes(s, device_sm_count()) > 0) return ATTN_PATH_PREFILL_SPLIT;
   return ATTN_PATH_PREFILL;
+}
+
+int attn_fwd_decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int paged, int sms, int ctas_per_sm,
+                         long long *info) {
+  if (info == nullptr) return -1;
+  const DecPlan pl = decode_plan_for(B, Hq, Hkv, Nq, Nk, d, paged != 0, sms, ctas_per_sm);
+  if (pl.bytes == 0) return -1;
+  info[0] = pl.nchunks;
+  info[1] = pl.chunk_keys;
+  info[2] = pl.fused ? 1 : 0;
+  info[3] = static_cast<long long>(pl.flag_off);
+  info[4] = static_cast<long long>(pl.bytes);
+  return 0;
 }
 
 int attn_fwd_prefill_visits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window,
