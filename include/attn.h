@@ -79,8 +79,9 @@ typedef enum {
   ATTN_PATH_SHORT = 2,         /* short-key kernel (Nk <= 128): one launch */
   ATTN_PATH_PREFILL_SPLIT = 3, /* tiled tcgen05 kernel, work split evenly over the
                                   SMs by K/V tiles (stream-K): one launch */
-  ATTN_PATH_SPLIT_KV_FUSED = 4 /* split-KV kernel whose last chunk of each query
-                                  group merges the group (small merges): one launch */
+  ATTN_PATH_SPLIT_KV_FUSED = 4 /* split-KV kernel whose last CTA to finish in each
+                                  query group merges the group (small merges): one
+                                  launch */
 } attn_path_t;
 
 /* Square attention, Nq = Nk = N.  Equivalent to attn_fwd_ex with Nq = Nk = N
@@ -107,7 +108,13 @@ attn_status_t attn_fwd(const void *Q, const void *K, const void *V, void *O, flo
  * in the CTA that holds the first keys of the rows.  When workspace is NULL
  * the non-split paths run.  When it is given it must hold at least
  * attn_fwd_workspace_bytes(...) bytes, 16-byte aligned, and must not be used
- * by another call that overlaps on the GPU.  The prefill split has the CTAs
+ * by another call that overlaps on the GPU.  Its contents need no
+ * initialisation: the split kernels' cross-CTA handshake words carry a tag
+ * of the enqueued call, and every launch leaves them cleared, so a CUDA
+ * graph that captured the call may replay it with new inputs written in
+ * place.  A launch that ends with ATTN_ERR_TIMEOUT may leave a prefill-split
+ * handshake word set: clear the workspace (all zero bytes) before a graph
+ * replays onto it again.  The prefill split has the CTAs
  * of one launch wait (bounded) for each other, so it expects its CTAs (one
  * per SM, at most the SM count) to be resident together; a concurrent
  * kernel that holds SMs for longer than the wait limit ends the call with
@@ -138,17 +145,18 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
  * are processed in parallel, then merged).  paged != 0 gives attn_fwd_paged's
  * plan (at most 2048 keys a chunk, max_seq_len = Nk).  info (HOST, 5
  * values, written): chunks per GQA group, keys per chunk (a multiple of 64;
- * the last chunk may be shorter), 1 when each group's last-chunk CTA merges
- * (one launch) else 0, byte offset of the merge flags in the workspace, and
- * the workspace bytes.  Returns 0, or -1 when the shape does not take the
+ * the last chunk may be shorter), 1 when each group's last CTA to finish
+ * merges (one launch) else 0, byte offset of the per-group arrival counters
+ * (8 bytes each) in the workspace, and the workspace bytes.  Returns 0, or -1 when the shape does not take the
  * split-KV path ((Hq / Hkv) * Nq > 32, B * Hkv > 65535, bad sizes). */
 int attn_fwd_decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int paged, int sms, int ctas_per_sm,
                          long long *info);
 
 /* The prefill kernel's schedule for these sizes, without device work: what
- * attn_fwd_ex would launch on a device of `sms` SMs (FlashAttention-2,
- * "Parallelism": query tiles of 128 rows as independent units, each walking
- * its live K/V tiles of 128 keys).  Only for shapes that take a prefill path
+ * attn_fwd_ex would launch on a device of `sms` SMs (lab 02, "La estructura
+ * del kernel": one program per batch x head and query tile, here query tiles
+ * of 128 rows as independent units, each walking its live K/V tiles of 128
+ * keys).  Only for shapes that take a prefill path
  * (ATTN_PATH_PREFILL or ATTN_PATH_PREFILL_SPLIT); returns -1 for invalid
  * sizes, a shape of another path or sms <= 0.
  *   info (HOST, 4 ints, written): grid (CTAs), schedule (0 one tile pass per
@@ -210,8 +218,8 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
 size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
 
 /* The path attn_fwd_paged takes for these sizes on the current device:
- * ATTN_PATH_SPLIT_KV_FUSED (each group's last-chunk CTA merges the chunks:
- * one launch) or ATTN_PATH_SPLIT_KV (a second, merge kernel); -1 when the
+ * ATTN_PATH_SPLIT_KV_FUSED (each group's last CTA to finish merges the
+ * chunks: one launch) or ATTN_PATH_SPLIT_KV (a second, merge kernel); -1 when the
  * sizes are invalid or the query group is too large.  The paged plan caps
  * the keys per chunk, since request lengths are known only on the device,
  * so it can split more finely than the flat call of max_seq_len keys.  No
@@ -242,6 +250,15 @@ attn_status_t attn_device_status(cudaStream_t stream);
  * later launches on any device (default 2e9).  0 restores the default. */
 void attn_set_wait_timeout_ns(unsigned long long ns);
 
+/* Test hook: in later launches on any device, the kernels' TMA producers
+ * stop loading after `tiles` K/V tiles (per CTA; for the short-key kernel,
+ * per unit of work) and wait for nothing more, so that the roles waiting for
+ * the missing tiles run into their bounded waits: the call still returns,
+ * with ATTN_ERR_TIMEOUT recorded for attn_device_status(), and its outputs
+ * are not valid.  A negative value (the default) turns the hook off.  For
+ * testing the error path only. */
+void attn_set_test_stall(int tiles);
+
 /* Static description of a status code. */
 const char *attn_status_string(attn_status_t status);
 
@@ -265,8 +282,11 @@ int attn_abi_version(void);
  *
  * The scratch array is a single 8 MiB block per GPU, reserved for as long as
  * the library is loaded.  Every call on a device uses the same block and
- * leaves its contents behind; nothing in it needs to start at zero, because
- * every value a call reads was written earlier in that call.  Calls whose
+ * leaves its contents behind; nothing in it needs to start at zero: every
+ * value a call reads was written earlier in that call, except the per-group
+ * arrival counters of the merge, which carry a tag of the call (a word with
+ * another tag counts as zero) and which the call leaves at zero arrivals.
+ * Calls whose
  * work overlaps on the GPU (different streams without ordering between them)
  * race on the block and give wrong results: order them on one stream.
  * The first call on a device looks up the block's device address; make that

@@ -63,7 +63,7 @@ def test_merge_and_workspace(attn, B, Hq, Hkv, Nq, Nk, d):
     assert p["fused"] == (1 if R * n * d <= 8192 else 0)
     part = B * Hq * Nq * n * (d + 1) * 4  # normalised partial O and its log2 LSE per (row, chunk)
     assert p["flag_off"] == (part + 15) // 16 * 16
-    assert p["bytes"] == p["flag_off"] + B * Hkv * n * 4  # one token flag per (group, chunk)
+    assert p["bytes"] == p["flag_off"] + B * Hkv * 8  # one tagged 64-bit arrival counter per group
 
 
 def test_paged_cap_splits_long_requests(attn):

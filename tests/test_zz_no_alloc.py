@@ -47,15 +47,18 @@ def call_with_workspace(attn, shape, q, k, v):
                                    workspace=ws)
 
 
-def test_two_calls_match_the_workspace_entry(attn):
-    # the decode workload (MQA, then GQA with 8 K/V heads): two calls in a row
+def test_two_calls_match_the_workspace_entry(attn, oracle_mod):
+    # the decode workload (MQA, then GQA with 8 K/V heads): two calls in a
+    # row, each also checked element by element against the fp64 oracle
     for idx in range(2):
         shape, cid, layer = ai.workload_calls("mqa_decode")[idx]
-        q, k, v = (t.cuda() for t in ai.make_qkv(shape, config_id=cid, layer=layer))
+        qh, kh, vh = ai.make_qkv(shape, config_id=cid, layer=layer)
+        q, k, v = qh.cuda(), kh.cuda(), vh.cuda()
         o_ref, lse_ref = call_with_workspace(attn, shape, q, k, v)
         o, lse = call_noalloc(attn, shape, q, k, v)
         assert (o.float() - o_ref.float()).abs().max().item() <= pu.TOL_O[shape.dtype]
         assert (lse - lse_ref).abs().max().item() <= pu.TOL_LSE
+        pu.check_full(shape, qh, kh, vh, o, lse, oracle_mod, f"no-alloc decode, call {idx + 1}")
 
 
 def test_second_call_with_other_inputs(attn):

@@ -36,7 +36,7 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
-            "attn_fwd_decode_plan"]
+            "attn_fwd_decode_plan", "attn_set_test_stall"]
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.attn_device_status.restype = ci
         L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
         L.attn_set_wait_timeout_ns.restype = None
+        L.attn_set_test_stall.argtypes = [ci]
+        L.attn_set_test_stall.restype = None
         L.attn_status_string.argtypes = [ci]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_abi_version.argtypes = []
@@ -176,6 +178,10 @@ def attn_device_status(stream) -> int:
 
 def attn_set_wait_timeout_ns(ns: int) -> None:
     lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def attn_set_test_stall(tiles: int) -> None:
+    lib().attn_set_test_stall(int(tiles))
 
 
 def attn_status_string(status: int) -> str:

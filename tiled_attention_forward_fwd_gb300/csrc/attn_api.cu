@@ -25,6 +25,7 @@ namespace attn {
 __device__ int g_status;
 
 static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+static std::atomic<int> g_stall_after{-1};  // attn_set_test_stall
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -145,6 +146,10 @@ static size_t split_plan_bytes(const Shape &s, int sms) {
   return split_ws_bytes(s.d, std::min(sms, kMaxSplitCtas));
 }
 
+// Tags of the split paths' cross-CTA handshakes (a fresh one per enqueued
+// call; a captured graph replays its own).  The handshake words are cleared
+// by the end of every launch, so a replay under the same tag starts from a
+// clean state; a tag never matches what other calls left in the memory.
 static std::atomic<unsigned> g_split_token{0};
 
 // One-time set-up of a prefill kernel on a device: its shared-memory size,
@@ -284,6 +289,7 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   }
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
+  p.stall_after = g_stall_after.load();
 
   auto kern = prefill_kernel<D, BF16>(sched);
   int dev = 0;
@@ -308,7 +314,7 @@ static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *
 struct DecPlan {
   int nchunks = 0, chunk_keys = 0;
   bool fused = false;    // the split kernel merges the chunks itself
-  size_t flag_off = 0;   // byte offset of the per-(group, chunk) flags
+  size_t flag_off = 0;   // byte offset of the per-group arrival counters (8 bytes each)
   size_t bytes = 0;      // 0: this shape does not take the split-KV path
 };
 
@@ -387,12 +393,12 @@ static DecPlan decode_plan_for(int B, int Hq, int Hkv, int Nq, int Nk, int d, bo
   pl.nchunks = (Nk + chunk_keys - 1) / chunk_keys;
   pl.chunk_keys = chunk_keys;
   // A small merge (rows x chunks x d of a group) is done by the split
-  // kernel's CTA of each group's last chunk; a large one by the merge kernel,
-  // one CTA per row.
+  // kernel's CTA that finishes last in each group (no CTA waits for
+  // another); a large one by the merge kernel, one CTA per row.
   pl.fused = R * pl.nchunks * d <= kDecFusedMerge;
   const size_t part = static_cast<size_t>(B) * Hq * Nq * pl.nchunks * (d + 1) * sizeof(float);
   pl.flag_off = (part + 15) & ~size_t(15);
-  pl.bytes = pl.flag_off + static_cast<size_t>(units) * pl.nchunks * sizeof(unsigned);
+  pl.bytes = pl.flag_off + static_cast<size_t>(units) * sizeof(unsigned long long);
   return pl;
 }
 
@@ -460,12 +466,13 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   p.kv_hi = s.Nk;
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
+  p.stall_after = g_stall_after.load();
   if (pl.fused) {
     p.fused = 1;
     unsigned tok = ++g_split_token;
     if (tok == 0) tok = ++g_split_token;
     p.token = tok;
-    p.flags = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(ws) + pl.flag_off);
+    p.counters = reinterpret_cast<unsigned long long *>(reinterpret_cast<uint8_t *>(ws) + pl.flag_off);
     p.O = O;
     p.lse = LSE;
   }
@@ -560,6 +567,7 @@ static attn_status_t launch_short_t(const void *Q, const void *K, const void *V,
   p.n_units = static_cast<int>(zq * p.n_qblocks);
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.timeout_ns = g_timeout_ns.load();
+  p.stall_after = g_stall_after.load();
   const int per_sm = short_ctas_per_sm<D, BF16, NK>(), sms = device_sm_count();
   if (per_sm <= 0 || sms <= 0) return ATTN_ERR_CUDA;
   const int grid = static_cast<int>(std::min<long long>(p.n_units, static_cast<long long>(per_sm) * sms));
@@ -815,6 +823,8 @@ attn_status_t attn_device_status(cudaStream_t stream) {
 
 void attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
 
+void attn_set_test_stall(int tiles) { g_stall_after.store(tiles < 0 ? -1 : tiles); }
+
 const char *attn_status_string(attn_status_t status) {
   switch (status) {
     case ATTN_OK: return "ok";
@@ -840,15 +850,23 @@ namespace attn {
 constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoallocScratchBytes];
 
-// Device address of the scratch block of the current device, looked up once
-// per device (with that device current).  nullptr if the lookup failed.
+// Device address of the scratch block of the current device, looked up with
+// that device current and kept once the lookup has succeeded.  nullptr if
+// it failed; the failure is not kept (a later call tries again), and its
+// error is cleared so that it is not reported by a later launch check.
 static float *noalloc_scratch(int dev) {
-  static std::once_flag once[64];
+  static std::mutex mu;
   static float *addr[64];
-  std::call_once(once[dev], [&] {
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
     void *ptr = nullptr;
-    addr[dev] = (cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess) ? static_cast<float *>(ptr) : nullptr;
-  });
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess) {
+      addr[dev] = static_cast<float *>(ptr);
+    } else {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+  }
   return addr[dev];
 }
 }  // namespace attn

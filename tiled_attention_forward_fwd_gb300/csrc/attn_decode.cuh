@@ -22,9 +22,12 @@
 // by more than 2^8.  At the end the 4 warps are merged in shared memory and
 // the chunk's normalised O and its log2-domain log-sum-exp go to the
 // caller's workspace.  When the merge is small (rows x chunks x d of a group
-// at most kDecFusedMerge floats), the CTA of a group's last chunk merges the
-// group's chunks itself once every chunk has published its partial (a flag
-// set to the launch's token with release semantics).  Otherwise kernel 2,
+// at most kDecFusedMerge floats), the last CTA of a group to finish merges
+// the group's chunks itself: every CTA counts its arrival on the group's
+// tagged counter after writing its partial, and the one that completes the
+// count (whichever chunk it holds) merges and clears the counter for the next
+// launch, so nothing waits and a CUDA graph can replay the launch.  Otherwise
+// kernel 2,
 // launched as a programmatic dependent so that its launch overlaps kernel 1,
 // merges the chunks of every row (one CTA per row) and writes O (16-bit) and
 // LSE.
@@ -56,7 +59,7 @@ constexpr int kDecMaxRows = 32;  // query rows of one group handled by one CTA
 constexpr int kDecMaxChunks = 1024;  // key chunks per group (bounds the merge kernel's shared memory)
 constexpr int kDecFusedMerge = 8192;  // rows x chunks x d of a group merged by the split kernel itself
 
-enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecWaitPartial = 0x202, kErrDecBadIndex = 0x203 };
+enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecBadIndex = 0x203 };
 
 struct DecParams {
   // flat: (d, Nk, B*Hkv), box 64 x 64 x 1; paged: (d, page_size,
@@ -66,11 +69,12 @@ struct DecParams {
   const void *Q;    // (B, Hq, Nq, d), 16-bit
   float *ws;        // [B*Hq*Nq][nchunks][d]: normalised O of each chunk
   float *ws_lse;    // [B*Hq*Nq][nchunks]: log2 LSE of each chunk (-inf: no live key)
-  // fused merge (fused != 0): flags [B*Hkv][nchunks] set to `token` once a
-  // chunk's partial is written; O and LSE written by the last chunk's CTA
+  // fused merge (fused != 0): one tagged arrival counter per group
+  // [B*Hkv] (tag = `token`, see arrive_tagged); O and LSE written by the
+  // group's last CTA to arrive
   int fused;
   unsigned token;
-  unsigned *flags;
+  unsigned long long *counters;
   void *O;
   float *lse;
   int *status;
@@ -80,6 +84,7 @@ struct DecParams {
   int kv_lo, kv_hi;  // keys any row of a group can see
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
+  int stall_after;  // test hook: the producer stops after this many K/V tiles (-1: never)
   // paged K/V: token t of request b sits in page block_table[b * max_pages +
   // t / page_size], slot t % page_size; request b holds seq_lens[b] tokens
   // (1..Nk, at least Nq when causal); kv_lo and kv_hi are not used
@@ -105,13 +110,14 @@ struct DecCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = ((kDecMaxRows * D * 2 + 1023) / 1024) * 1024;
   static constexpr int kStageBytes = 2 * kTileBytes;        // K then V
-  static constexpr int kOffBar = kOffKV + kStages * kStageBytes;  // kfull, vfull, kempty, vempty [stages]; abort
+  // kfull, vfull, kempty, vempty [stages]; abort flag; the group counter as first read
+  static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
   static constexpr int kOffStats = kOffBar + 256;           // float wm[4][32], wl[4][32], rinv[32]
   static constexpr int kSmemBytes = kOffStats + (2 * kDecWarps + 1) * kDecMaxRows * 4 + 1024;
   static constexpr int kSlabStride = D + 8;                 // floats per merge-slab row (2-way bank conflicts)
   static_assert(kDecWarps * kDecMaxRows * kSlabStride * 4 <= kStages * kStageBytes,
                 "O merge slabs fit in the ring");
-  static_assert(4 * kStages * 8 + 4 <= 256, "barriers fit");
+  static_assert(4 * kStages * 8 + 16 <= 256, "barriers fit");
   static_assert(kMinCtas * (kSmemBytes + 1024) <= 233472, "shared memory per SM");
 };
 
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   int *abort_flag = reinterpret_cast<int *>(bars + 4 * NS);
+  unsigned long long *ctr_seen = reinterpret_cast<unsigned long long *>(bars + 4 * NS + 1);
   float *wm = reinterpret_cast<float *>(smem + C::kOffStats);  // [warp][row] running max (log2 domain)
   float *wl = wm + kDecWarps * kDecMaxRows;                    // [warp][row] running sum
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
@@ -201,6 +208,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
   }
   __syncthreads();
   pdl_wait();  // inputs may come from the previous kernel on the stream
+  // the fused merge's group counter, read now (its latency hides behind the
+  // keys) by the producer warp
+  if (p.fused && threadIdx.x == 32 * kDecWarps) *ctr_seen = ld_relaxed_gpu_u64(p.counters + bk);
   bool ok = true;
   // keys of this request, and the ones this chunk takes
   int nk = p.kv_hi, kv_lo = p.kv_lo;
@@ -246,6 +256,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
     int page_next = (kPaged && ntiles > 0) ? read_page(0) : 0;
     int kiss = 0, viss = 0;  // K / V tiles issued
     for (int i = 0; i < ntiles; ++i) {
+      if (p.stall_after >= 0 && i >= p.stall_after) {  // test hook: stop loading
+        ok = false;
+        break;
+      }
       const int s = i % NS, y = k0 + i * kDecKeys;
       const uint32_t kdst = sKV + s * C::kStageBytes, vdst = kdst + C::kTileBytes;
       int slab[kMaxTilePages];
@@ -454,91 +468,96 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
     if (lane == 0) mbar_arrive(bVempty(s));  // this warp is done with V of tile i
   }
   // Every thread learns whether any role gave up; then nothing is in flight
-  // (the producer drained its copies above) and the CTA can leave.
-  if (__syncthreads_or(!ok)) return;
-
-  // ---- merge the 4 warps: row sums over the quad, then max / sums per row in shared memory
-  const bool consumer = warp < kDecWarps;
+  // (the producer drained its copies above).  A CTA that gave up writes no
+  // partial, but still counts its arrival in a fused merge (below), so that
+  // the group's counter is cleared at the end of the launch as always.
+  const bool failed = __syncthreads_or(!ok);
+  if (failed && !p.fused) return;
+  // O slabs, one per warp ([warp][32][kSlabStride]; the ring is idle now)
+  float *oacc = reinterpret_cast<float *>(smem + C::kOffKV);
+  if (!failed) {
+    // ---- merge the 4 warps: row sums over the quad, then max / sums per row in shared memory
+    const bool consumer = warp < kDecWarps;
 #pragma unroll
-  for (int rb = 0; rb < RB; ++rb)
+    for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      l[rb][h] += __shfl_xor_sync(0xffffffffu, l[rb][h], 1);
-      l[rb][h] += __shfl_xor_sync(0xffffffffu, l[rb][h], 2);
-      if (consumer && tq == 0) {
-        const int r = rb * 16 + g + 8 * h;
-        wm[warp * kDecMaxRows + r] = m[rb][h];
-        wl[warp * kDecMaxRows + r] = l[rb][h];
+      for (int h = 0; h < 2; ++h) {
+        l[rb][h] += __shfl_xor_sync(0xffffffffu, l[rb][h], 1);
+        l[rb][h] += __shfl_xor_sync(0xffffffffu, l[rb][h], 2);
+        if (consumer && tq == 0) {
+          const int r = rb * 16 + g + 8 * h;
+          wm[warp * kDecMaxRows + r] = m[rb][h];
+          wl[warp * kDecMaxRows + r] = l[rb][h];
+        }
       }
-    }
-  // one slab per warp, summed in a fixed order below (deterministic result)
-  float *oacc = reinterpret_cast<float *>(smem + C::kOffKV);  // [warp][32][kSlabStride], the ring is idle now
-  float *rinv = wl + kDecWarps * kDecMaxRows;                  // [row] 1 / (chunk sum)
-  __syncthreads();
+    // each warp's O into its slab, summed in a fixed order below (deterministic result)
+    float *rinv = wl + kDecWarps * kDecMaxRows;  // [row] 1 / (chunk sum)
+    __syncthreads();
 #pragma unroll
-  for (int rb = 0; rb < RB; ++rb)
+    for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (!consumer) continue;
-      const int r = rb * 16 + g + 8 * h;
+      for (int h = 0; h < 2; ++h) {
+        if (!consumer) continue;
+        const int r = rb * 16 + g + 8 * h;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * kDecMaxRows + r]);
+        const float scale = (m[rb][h] == -INFINITY) ? 0.f : ex2_approx(m[rb][h] - M);
+        float *slab = oacc + (warp * kDecMaxRows + r) * C::kSlabStride;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2 *>(slab + n * 8 + 2 * tq) =
+              make_float2(o[rb][n][2 * h] * scale, o[rb][n][2 * h + 1] * scale);
+      }
+    // per-row totals, once per row: the chunk's log2 LSE and 1 / sum
+    if (threadIdx.x < p.R) {
+      const int r = threadIdx.x;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * kDecMaxRows + r]);
-      const float scale = (m[rb][h] == -INFINITY) ? 0.f : ex2_approx(m[rb][h] - M);
-      float *slab = oacc + (warp * kDecMaxRows + r) * C::kSlabStride;
+      float L = 0.f;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n)
-        *reinterpret_cast<float2 *>(slab + n * 8 + 2 * tq) =
-            make_float2(o[rb][n][2 * h] * scale, o[rb][n][2 * h + 1] * scale);
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = wm[w * kDecMaxRows + r];
+        if (mw != -INFINITY) L += ex2_approx(mw - M) * wl[w * kDecMaxRows + r];
+      }
+      rinv[r] = (L > 0.f) ? 1.f / L : 0.f;
+      const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
+      const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
+      p.ws_lse[grow * p.nchunks + chunk] = (L > 0.f) ? M + log2f(L) : -INFINITY;
     }
-  // per-row totals, once per row: the chunk's log2 LSE and 1 / sum
-  if (threadIdx.x < p.R) {
-    const int r = threadIdx.x;
-    float M = -INFINITY;
+    __syncthreads();
+    // ---- this chunk's normalised O -> workspace, four columns per thread
+    for (int idx = threadIdx.x; idx < p.R * (D / 4); idx += kDecThreads) {
+      const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+      float4 acc = *reinterpret_cast<const float4 *>(oacc + r * C::kSlabStride + c);
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * kDecMaxRows + r]);
-    float L = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float mw = wm[w * kDecMaxRows + r];
-      if (mw != -INFINITY) L += ex2_approx(mw - M) * wl[w * kDecMaxRows + r];
+      for (int w = 1; w < kDecWarps; ++w) {
+        const float4 v = *reinterpret_cast<const float4 *>(oacc + (w * kDecMaxRows + r) * C::kSlabStride + c);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const float inv = rinv[r];
+      const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
+      const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
+      *reinterpret_cast<float4 *>(p.ws + (grow * p.nchunks + chunk) * D + c) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
-    rinv[r] = (L > 0.f) ? 1.f / L : 0.f;
-    const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
-    const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
-    p.ws_lse[grow * p.nchunks + chunk] = (L > 0.f) ? M + log2f(L) : -INFINITY;
-  }
-  __syncthreads();
-  // ---- this chunk's normalised O -> workspace, four columns per thread
-  for (int idx = threadIdx.x; idx < p.R * (D / 4); idx += kDecThreads) {
-    const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
-    float4 acc = *reinterpret_cast<const float4 *>(oacc + r * C::kSlabStride + c);
-#pragma unroll
-    for (int w = 1; w < kDecWarps; ++w) {
-      const float4 v = *reinterpret_cast<const float4 *>(oacc + (w * kDecMaxRows + r) * C::kSlabStride + c);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const float inv = rinv[r];
-    const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
-    const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
-    *reinterpret_cast<float4 *>(p.ws + (grow * p.nchunks + chunk) * D + c) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   if (!p.fused) return;
-  // ---- fused merge: publish this chunk; the group's last chunk merges
-  __syncthreads();  // every thread's partial is written before the one release
-  unsigned *fl = p.flags + static_cast<size_t>(bk) * p.nchunks;
-  if (threadIdx.x == 0) st_release_gpu(fl + chunk, p.token);
-  if (chunk != p.nchunks - 1) return;
-  // The other chunks of the group have lower block indices: they were
-  // launched before this CTA and wait for nothing of it.
-  bool got = true;
-  for (int c = threadIdx.x; c < p.nchunks - 1; c += kDecThreads)
-    got = got && flag_wait(fl + c, p.token, wc, kErrDecWaitPartial);
-  if (__syncthreads_or(!got)) return;
+  // ---- fused merge: the group's last CTA to arrive merges (no waiting)
+  __syncthreads();  // every thread's partial is written before the one arrival
+  bool last = false;
+  if (threadIdx.x == 0) {
+    unsigned long long *ctr = p.counters + bk;
+    last = arrive_tagged(ctr, *ctr_seen, p.token, static_cast<unsigned>(p.nchunks));
+    if (last) reset_tagged(ctr, p.token);  // every chunk has arrived: ready for the next launch
+  }
+  // the last arriver's thread 0 acquired every chunk's partial; the barrier
+  // orders its threads' reads (L2, __ldcg) after that
+  if (!__syncthreads_or(last) || failed) return;
   // per row: the chunk weights 2^(lse_c - M) and 1 / their sum (shared
   // memory: the ring is idle)
   float *linv = oacc;               // [R]

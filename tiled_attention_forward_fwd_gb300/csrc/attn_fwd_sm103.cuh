@@ -73,12 +73,16 @@ struct FwdParams {
   FastDiv fd_group;  // / group
   float scale_log2;  // sm_scale * log2(e)
   unsigned long long timeout_ns;
+  int stall_after;  // test hook: the producer stops after this many K/V tiles (-1: never)
   // Stream-K split (the kSchedSplit kernel): the items, in order, form one
   // sequence of K/V tile steps (each item its union range); CTA c takes the
   // steps from split_at[c] to split_at[c + 1] (x = item, y = step within the
   // item).  An item cut between CTAs is finished by the CTA holding its first
   // steps: the others leave their partial O (fp32, not normalised) and (m, l)
-  // per row in the workspace and set their flag to `token`.
+  // per row in the workspace and set their flag to `token` (fresh per
+  // enqueued call, so it never matches what other calls left there); the
+  // merging CTA clears each flag it consumed, so a graph replay under the
+  // same token waits for its own partials.
   unsigned token;
   float *ws_o;        // [CTA][tile][D][128 rows]: a warp's 32 rows of one column are contiguous
   float2 *ws_ml;      // [CTA][tile][128 rows]
@@ -487,6 +491,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         for (int k = 0; ok && k < it.uend - it.ubeg; ++k) {
           const int j = ring_block<kHalves>(it, k);  // K/V tile of ring position k
           const int c = ckv, s = c % NS;
+          if (p.stall_after >= 0 && c >= p.stall_after) {  // test hook: stop loading
+            ok = false;
+            break;
+          }
           if (c >= NS && !mbar_wait_warp(bKVempty(s), ((c / NS) - 1) & 1, wc, kErrWaitKVEmpty)) {
             ok = false;
             break;
@@ -549,8 +557,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         if (ok && elect_one()) umma_commit(bKVempty(c % NS));
         __syncwarp();
       };
+      // After an abort (ok false) no MMA is issued, but S full, P V done and
+      // O final are still signalled, by a plain arrival: the softmax
+      // warpgroup keeps waiting for them, so that it never arrives at a
+      // handoff barrier before this warp has passed that barrier's previous
+      // phase (an arrive-only side that ran ahead could complete a phase
+      // without this warp and leave its next sync waiting forever), and so
+      // that no P V done phase is left pending into the next item (O final
+      // completes with the item's last one).
       auto issue_qk = [&](int c, int qbuf, bool last) {
-        if (!ok) return;
+        if (!ok) {
+          if (elect_one()) mbar_arrive(bSfull(t));
+          __syncwarp();
+          return;
+        }
         tc_fence_after();
         const uint64_t qd = sdesc_sw128(sQ + (t * QB + qbuf) * C::kQBytes, 16, 1024);
         const uint64_t kd = sdesc_sw128(sK + (c % NS) * C::kTileBytes, 16, 1024);
@@ -563,7 +583,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       };
       auto issue_pv = [&]() {
         named_bar_sync(kBarP + t, kBarHandoffThreads);
-        ok = ok && *reinterpret_cast<volatile int *>(abort_flag) == 0;
+        ok = ok && !__any_sync(0xffffffffu, *reinterpret_cast<volatile int *>(abort_flag) != 0);
+        if (!ok) {
+          if (elect_one()) {
+            if constexpr (C::kSeparateP) mbar_arrive(bPVdone(t));
+            if (pv_last) mbar_arrive(bOfinal(t));
+          }
+          __syncwarp();
+        }
         if (ok) {
           tc_fence_after();
           const uint64_t vd = sdesc_sw128(sV + pv_stage * C::kTileBytes, C::kBoxBytes, 1024);
@@ -682,19 +709,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       float m = -INFINITY;  // running max of scaled scores, log2 domain (may lag by < 2^8)
       float l = 0.f;        // running sum of exp2(s * sl2 - m), fp32
       for (int j = tbeg; j < tend; ++j) {
-        // After a failed wait the work is skipped but the barriers are not.
-        ok = ok && mbar_wait_warp(bSfull(t), ns & 1, wc, kErrWaitS);
+        // The MMA warp signals S full and P V done after an abort too
+        // (without MMAs then), so these waits do not poll the abort flag
+        // and are always taken, and the block's work always runs (on
+        // whatever S holds after an abort): this warpgroup then never
+        // arrives at a handoff barrier before the MMA warp has passed that
+        // barrier's previous phase.
+        ok = mbar_wait_signal(bSfull(t), ns & 1, wc, kErrWaitS) && ok;
         ns++;
         uint32_t sr[kBN];
-        if (ok) {
-          tc_fence_after();
-          tmem_ld128(scol, sr);
-        }
+        tc_fence_after();
+        tmem_ld128(scol, sr);
         if constexpr (C::kSeparateP) {
           tc_fence_before();
           named_bar_arrive(kBarSRead + t, kBarHandoffThreads);  // S_t(j) read: the next Q K^T may overwrite it
         }
-        if (ok) {
+        {
           const int key0 = j * kBN;
           const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
                                  (p.window > 0 && key0 <= p1 - p.window);
@@ -716,7 +746,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           auto before_store = [&]() {
             if constexpr (C::kSeparateP) {
               if (!pv_waited) {
-                ok = mbar_wait_warp(bPVdone(t), (npv - 1) & 1, wc, kErrWaitS) && ok;
+                ok = mbar_wait_signal(bPVdone(t), (npv - 1) & 1, wc, kErrWaitS) && ok;
                 pv_waited = true;
               }
               tc_fence_after();
@@ -820,6 +850,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
             mf = mn;
           }
         }
+        // each thread waited on its own: the warp agrees before the
+        // warp-collective TMEM loads that ok guards
+        ok = __all_sync(0xffffffffu, ok);
       }
       float a_own = (m == -INFINITY) ? 0.f : ex2_approx(m - mf);  // 1 unless merged
       float inv = part_out ? 1.f : ((lf > 0.f) ? 1.f / lf : 0.f);
@@ -827,7 +860,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         p.lse[static_cast<size_t>(tbh) * p.Nq + grow] =
             ((lf > 0.f) ? mf + log2f(lf) : -INFINITY) * 0.69314718055994530942f;
       const int qbuf = nfin % QB;  // this item's Q buffer (the MMA warp counts items the same way)
-      ok = ok && mbar_wait_warp(bOfinal(t), nfin & 1, wc, kErrWaitOFinal);
+      // O final: also a signal wait (given after an abort too); it covers the
+      // item's last P V done, which no block of the item waits for
+      ok = mbar_wait_signal(bOfinal(t), nfin & 1, wc, kErrWaitOFinal) && ok;
       nfin++;
       // kPairHalves: tile 0's (m, l) go through shared memory, its final O is
       // read by tile 1 straight from TMEM (same lanes: same rows)
@@ -962,6 +997,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           }
         }
         half_read_done();
+      }
+      if constexpr (kSplit) {
+        if (merge_in) {
+          // Every thread of the warpgroup is past its flag waits (and no
+          // piece writes its flag twice in a launch): clear the flags read,
+          // so that the next launch on this workspace, a CUDA graph replay
+          // under the same token included, waits for fresh partials.
+          named_bar_sync(kBarOStaged + t, 128);
+          if (quad == 0 && lane == 0)
+            for (int c = blockIdx.x + 1; c < static_cast<int>(gridDim.x) && p.split_at[c].x == ie.item; ++c)
+              if (part_live(c)) st_relaxed_gpu(p.ws_flag + c * 2 + t, 0u);
+          __syncwarp();
+        }
       }
       // The next item's first P V (accumulate = 0) overwrites O_t; it is
       // issued only after the next P barrier, which these warps reach after

@@ -42,6 +42,7 @@ struct ShortParams {
   int n_units;    // B * Hq * n_qblocks
   float scale_log2;
   unsigned long long timeout_ns;
+  int stall_after;  // test hook: the producer stops after this many K/V tiles (-1: never)
 };
 
 // Ring depth and resident CTAs per SM: about 190 KB of loads in flight per SM.
@@ -104,6 +105,10 @@ __global__ void __launch_bounds__(kShortThreads, ShortCfg<D, NK>::kMinCtas)
     __syncwarp();
     int n = 0;
     for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++n) {
+      if (p.stall_after >= 0 && n >= p.stall_after) {  // test hook: stop loading
+        ok = false;
+        break;
+      }
       const int s = n % NS;
       if (n >= NS && !mbar_wait_warp(bEmpty(s), ((n / NS) - 1) & 1, wc, kErrShortWait)) {
         ok = false;

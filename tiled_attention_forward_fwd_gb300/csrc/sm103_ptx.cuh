@@ -108,19 +108,25 @@ struct WaitCtl {
 };
 
 // Bounded wait by the calling thread.  Returns false on timeout or when some
-// other role of the CTA has already aborted.
+// other role of the CTA has already aborted.  The limit and the abort flag
+// are checked after every failed poll (mbarrier.try_wait itself suspends
+// the thread for a while before it reports failure, so a poll is never a
+// tight spin).  The limit is counted in SM clock cycles, 3 per nanosecond
+// (cheaper to read than the global timer; at clocks up to 3 GHz the wait
+// lasts at least the limit).
+__device__ __forceinline__ bool past_limit(long long t0, uint64_t limit_ns) {
+  return static_cast<unsigned long long>(clock64() - t0) > 3ull * limit_ns;
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w, int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  const long long t0 = clock64();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.timeout_ns) {
-        *w.abort_flag = 1;
-        atomicCAS(w.status, 0, code);
-        return false;
-      }
+    if (*w.abort_flag) return false;
+    if (past_limit(t0, w.timeout_ns)) {
+      *w.abort_flag = 1;
+      atomicCAS(w.status, 0, code);
+      return false;
     }
   }
 }
@@ -134,21 +140,73 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
 __device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed_gpu(unsigned *p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel_gpu_u64(unsigned long long *p,
+                                                                       unsigned long long expect,
+                                                                       unsigned long long desired) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(p), "l"(expect), "l"(desired)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu_u64(unsigned long long *p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
+// Arrival of one of `n` CTAs at a tagged counter in global memory: the high
+// 32 bits hold the tag of the launch (nonzero), the low 32 bits the arrivals
+// counted under that tag.  `seen` is the word as the CTA read it earlier in
+// the launch (any time after the previous kernel on the stream finished).
+// A word with another tag (left by another call, or whatever the memory held
+// before its first use) is first restarted at (tag, 0) by one
+// compare-and-swap against `seen`, which can succeed only while no arrival of
+// this launch has been counted; then every arrival adds one.  Returns true
+// for the arrival that completes the count (exactly one of the n), which
+// leaves the word at (tag, 0) again (reset_tagged), so that the next launch
+// under the same tag (a CUDA graph replays the tag it was captured with)
+// only adds.  The add has release and acquire semantics at GPU scope: the
+// caller's writes (and those its CTA ordered before the arrival with a
+// barrier) are visible to the last arriver, which sees every earlier
+// arriver's writes.  No loop: at most one compare-and-swap, one add.
+__device__ __forceinline__ bool arrive_tagged(unsigned long long *word, unsigned long long seen, unsigned tag,
+                                              unsigned n) {
+  if (static_cast<unsigned>(seen >> 32) != tag)
+    atom_cas_acq_rel_gpu_u64(word, seen, static_cast<unsigned long long>(tag) << 32);
+  const unsigned long long old = atom_add_acq_rel_gpu_u64(word, 1ull);
+  return static_cast<unsigned>(old >> 32) == tag && static_cast<unsigned>(old) == n - 1;
+}
+// The last arriver's reset: (tag, 0), ready for the next launch under the tag.
+__device__ __forceinline__ void reset_tagged(unsigned long long *word, unsigned tag) {
+  st_relaxed_gpu_u64(word, static_cast<unsigned long long>(tag) << 32);
+}
 
 // Bounded wait of the calling thread for *flag == value (set by another CTA
 // of the same grid).  Returns false on timeout or when the CTA has aborted.
 __device__ __forceinline__ bool flag_wait(const unsigned *flag, unsigned value, const WaitCtl &w, int code) {
   if (ld_acquire_gpu(flag) == value) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  const long long t0 = clock64();
+  for (;;) {
     if (ld_acquire_gpu(flag) == value) return true;
-    if ((it & 31u) == 0) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.timeout_ns) {
-        *w.abort_flag = 1;
-        atomicCAS(w.status, 0, code);
-        return false;
-      }
+    if (*w.abort_flag) return false;
+    if (past_limit(t0, w.timeout_ns)) {
+      *w.abort_flag = 1;
+      atomicCAS(w.status, 0, code);
+      return false;
     }
   }
 }
@@ -158,19 +216,37 @@ __device__ __forceinline__ bool flag_wait(const unsigned *flag, unsigned value, 
 // .sync.aligned tcgen05 instructions that follow.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl &w, int code) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const bool aborted = *w.abort_flag != 0;
+    const bool late = past_limit(t0, w.timeout_ns);
+    if (__any_sync(0xffffffffu, aborted || late)) {
+      if ((threadIdx.x & 31) == 0 && !aborted) {
+        *w.abort_flag = 1;
+        atomicCAS(w.status, 0, code);
+      }
+      return false;
+    }
+  }
+}
+
+// Warp-collective wait for a signal that another role of the CTA gives in
+// every case, after an abort too (without work then): it does not poll the
+// abort flag, and its bound is the larger of the wait limit and 1 s.  On
+// that bound it records `code` like any wait and returns false.
+__device__ __forceinline__ bool mbar_wait_signal(uint32_t bar, uint32_t parity, const WaitCtl &w, int code) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = w.timeout_ns > 1000000000ull ? w.timeout_ns : 1000000000ull;
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    if ((it & 31u) == 0) {
-      const bool aborted = *w.abort_flag != 0;
-      const bool late = globaltimer_ns() - t0 > w.timeout_ns;
-      if (__any_sync(0xffffffffu, aborted || late)) {
-        if ((threadIdx.x & 31) == 0 && !aborted) {
-          *w.abort_flag = 1;
-          atomicCAS(w.status, 0, code);
-        }
-        return false;
+    if ((it & 31u) == 0 && __any_sync(0xffffffffu, globaltimer_ns() - t0 > limit)) {
+      if ((threadIdx.x & 31) == 0) {
+        *w.abort_flag = 1;
+        atomicCAS(w.status, 0, code);
       }
+      return false;
     }
   }
 }
