@@ -48,7 +48,8 @@ def test_mqa_decode_workload(attn, oracle_mod, idx):
     shape, cid, layer = ai.workload_calls("mqa_decode")[idx]
     q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
     o, lse = run_split(attn, shape, q, k, v)
-    pu.check_full(shape, q, k, v, o, lse, oracle_mod, f"mqa_decode {idx}")
+    pu.check_full(shape, q, k, v, o, lse, oracle_mod, f"mqa_decode {idx}",
+                  config=f"C-dec mqa_decode B4 Hq32 Hkv{shape.Hkv} Nq1 Nk8192 d128 causal", strict=True)
 
 
 @pytest.mark.parametrize("Nk", [1, 2, 63, 64, 65, 129, 1000, 5000])

@@ -41,13 +41,14 @@ def run_paged(attn, shape, q, k, v, table, lens, ws_extra=0):
     return o, lse
 
 
-def check(attn, oracle_mod, shape, cid, layer=0):
+def check(attn, oracle_mod, shape, cid, layer=0, config=None, strict=False):
     q, k, v, table, lens = ai.make_paged(shape, cid, layer)
     o, lse = run_paged(attn, shape, q, k, v, table, lens)
     kw = dict(causal=shape.causal, window=shape.window, sm_scale=shape.scale)
     o_ref, lse_ref = oracle_mod.attention_paged(q, k, v, table, lens, **kw)
     a_ref, _ = oracle_mod.attention_paged(q, k, v.abs(), table, lens, **kw)
-    pu.compare(shape.dtype, o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref, str(shape), a_ref)
+    pu.compare(shape.dtype, o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref, str(shape), a_ref, config,
+               strict)
     return q, k, v, table, lens, o, lse
 
 
@@ -81,7 +82,7 @@ def test_window(attn, oracle_mod, window):
 @pytest.mark.parametrize("Hq,Hkv,Nq,max_len", [(32, 1, 1, 9000), (16, 2, 4, 6000), (4, 4, 1, 20000)])
 def test_merge_paths(attn, oracle_mod, Hq, Hkv, Nq, max_len):
     """Groups of 32 rows over many chunks (the separate merge kernel) and
-    small groups (the merge done by each group's last-chunk CTA)."""
+    small groups (the merge done by the last CTA of each group to finish)."""
     shape = ai.PagedShape(3, Hq, Hkv, Nq, max_len, 128, 16, "bf16", True, 0, None, None, max_len // 2, 2)
     check(attn, oracle_mod, shape, 103, Hq + Nq)
 
@@ -190,7 +191,8 @@ def test_workload_full_size(attn, oracle_mod, idx):
     """The benchmark's paged_decode calls at full size, every row against the
     oracle."""
     shape, cid, layer = ai.workload_calls("paged_decode")[idx]
-    check(attn, oracle_mod, shape, cid, layer)
+    check(attn, oracle_mod, shape, cid, layer,
+          config=f"C-dec paged_decode B{shape.B} Hq32 Hkv8 Nq1 L{shape.max_seq_len} ps16 d128 causal", strict=True)
 
 
 def test_paged_plan(attn):

@@ -19,23 +19,28 @@ def attn():
     return m
 
 
-def _run_and_check(shape, oracle_mod, config_id=50, layer=0, label=""):
+def _run_and_check(shape, oracle_mod, config_id=50, layer=0, label="", config=None, strict=False):
     q, k, v = ai.make_qkv(shape, config_id=config_id, layer=layer)
     o, lse = pu.run_cuda(shape, q, k, v)
-    return pu.check_full(shape, q, k, v, o, lse, oracle_mod, label or str(shape))
+    return pu.check_full(shape, q, k, v, o, lse, oracle_mod, label or str(shape), config, strict)
+
+
+def _name(workload, shape):
+    return (f"{workload} B{shape.B} Hq{shape.Hq} Hkv{shape.Hkv} Nq{shape.Nq} Nk{shape.Nk} d{shape.d}"
+            f"{' causal' if shape.causal else ''}{f' w{shape.window}' if shape.window else ''}")
 
 
 # ------------------------------------------------------------------ the stated workloads (small ones in full)
 @pytest.mark.parametrize("idx", [0, 1])
 def test_mha_n64(attn, oracle_mod, idx):
     shape, cid, layer = ai.workload_calls("mha_n64")[idx]
-    _run_and_check(shape, oracle_mod, cid, layer)
+    _run_and_check(shape, oracle_mod, cid, layer, config=_name("C1 mha_n64", shape), strict=True)
 
 
 @pytest.mark.parametrize("idx", range(6))
 def test_mha_b2h4(attn, oracle_mod, idx):
     shape, cid, layer = ai.workload_calls("mha_b2h4")[idx]
-    _run_and_check(shape, oracle_mod, cid, layer)
+    _run_and_check(shape, oracle_mod, cid, layer, config=_name("C2 mha_b2h4", shape), strict=True)
 
 
 # ------------------------------------------------------------------ ragged and tiny shapes
@@ -169,7 +174,8 @@ def test_gpt_stack_full_size(attn, oracle_mod, layer):
     q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
     o, lse = pu.run_cuda(shape, q, k, v)
     pu.check_properties(shape, v, o, lse)
-    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=512, seed=layer, label=f"gpt layer {layer}")
+    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=512, seed=layer, label=f"gpt layer {layer}",
+                     config=_name(f"C3 gpt_stack layer {layer}", shape) + " (512 sampled rows)", strict=True)
 
 
 @pytest.mark.parametrize("idx", [0, 1, 2])
@@ -178,7 +184,8 @@ def test_gqa_mqa_full_size(attn, oracle_mod, idx):
     q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
     o, lse = pu.run_cuda(shape, q, k, v)
     pu.check_properties(shape, v, o, lse)
-    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=512, seed=idx, label=f"gqa_mqa {idx}")
+    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=512, seed=idx, label=f"gqa_mqa {idx}",
+                     config=_name("C4 gqa_mqa", shape) + " (512 sampled rows)", strict=shape.window == 0)
 
 
 def test_long_prefill_full_size(attn, oracle_mod):
@@ -186,5 +193,6 @@ def test_long_prefill_full_size(attn, oracle_mod):
     q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
     o, lse = pu.run_cuda(shape, q, k, v)
     pu.check_properties(shape, v, o, lse)
-    stats = pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=768, seed=4, label="long prefill")
+    stats = pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=768, seed=4, label="long prefill",
+                             config=_name("C5 long_prefill", shape) + " (768 sampled rows)")
     print("long_prefill", stats)

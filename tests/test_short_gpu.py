@@ -65,4 +65,6 @@ def test_mha_n64_bandwidth_full_size(attn, oracle_mod, idx):
     q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
     o, lse = pu.run_cuda(shape, q, k, v)
     pu.check_properties(shape, v.cuda(), o, lse)
-    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=1024, label="mha_n64_bw")
+    pu.check_sampled(shape, q, k, v, o, lse, oracle_mod, count=1024, label="mha_n64_bw",
+                     config=f"C1-bw mha_n64_bw B512 H32 N64 d64{' causal' if shape.causal else ''} (1024 rows)",
+                     strict=True)
