@@ -4,13 +4,17 @@ of the dominant kernel, next to the fp64 CPU oracle timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass over every call of the workload (default ``mha_b2h4``:
-B=2, H=4, d=64, fp16, N in {256, 1024, 4096} x causal in {true, false}) with
-inputs resident in HBM.  The step is captured once as a CUDA graph and
+A step is one pass over every call of the workload with inputs resident in
+HBM.  The default workload is the largest single-GPU configuration,
+``long_prefill``: B=1, Hq=32, Hkv=8, N=32768, d=128, bf16, keys x3, causal
+(8.8 TFLOP per step).  The step is captured once as a CUDA graph and
 replayed; L2 is flushed between timed steps, outside the timed events: a
 256 MiB write, then a 256 MiB read of another buffer, so that the timed step
 starts with none of its inputs in L2 and with no dirty lines of the flush
-left to write back.  Prints one JSON line (rank 0).
+left to write back.  Before the timed steps, after the warm-up steps,
+untimed replays run for at least a second (the soak), so that the clocks
+sampled during the timed region are those of a GPU under load.  Prints one
+JSON line (rank 0).
 """
 from __future__ import annotations
 
@@ -60,14 +64,16 @@ KERNEL_SOURCES = {
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mha_b2h4", choices=ai.WORKLOAD_NAMES)
+    ap.add_argument("--workload", default="long_prefill", choices=ai.WORKLOAD_NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--per-call", action="store_true", help="print per-call timings to stderr")
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="untimed replays after the warm-up, before the timed steps")
     return ap.parse_args()
 
 
@@ -307,7 +313,7 @@ def build_graph(calls, stream, per_call_events: bool):
     return g, evs
 
 
-def device_timing(calls, steps, warmup, device, stream):
+def device_timing(calls, steps, warmup, device, stream, soak_s=1.0):
     import tiled_attention_forward_fwd_gb300 as attn
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
@@ -327,6 +333,15 @@ def device_timing(calls, steps, warmup, device, stream):
             flush_l2()
             g_calls.replay()
     torch.cuda.synchronize(device)
+    soak = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < soak_s:
+        with torch.cuda.stream(stream):
+            for _ in range(4):
+                flush_l2()
+                g.replay()
+                soak += 1
+        stream.synchronize()
     step_ms, call_ms = [], [[] for _ in calls]
     for _ in range(steps):
         with torch.cuda.stream(stream):
@@ -347,7 +362,7 @@ def device_timing(calls, steps, warmup, device, stream):
     st = attn.attn_device_status(stream.cuda_stream)
     if st != attn.ATTN_OK:
         raise RuntimeError(f"kernel status after timing: {attn.attn_status_string(st)}")
-    return step_ms, call_ms
+    return step_ms, call_ms, soak
 
 
 def e2e_timing(calls, steps, warmup, device, stream):
@@ -550,7 +565,7 @@ def main():
     torch.cuda.synchronize(device)
     sampler = ClockSampler(local)
     sampler.start()
-    step_ms, call_ms = device_timing(calls, steps, warmup, device, stream)
+    step_ms, call_ms, soak_steps = device_timing(calls, steps, warmup, device, stream, args.soak_seconds)
     clocks = sampler.stop()
     torch.cuda.synchronize(device)
     dist_barrier(ws)
@@ -572,6 +587,8 @@ def main():
         achieved = dc["flops"] / (avg[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                 "frac": achieved / peak_t}
+        if "bf16_tflops_sustained" in peaks:  # context: the power-capped rate of a seconds-long GEMM loop
+            roof["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
     else:
         achieved = dc["bytes"] / (avg[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -611,6 +628,7 @@ def main():
                        "flop_convention": "4*B*Hq*N^2*d, halved for square causal; exact live pairs otherwise",
                        "l2": "flushed between timed steps outside the timed events: 256 MiB write, then 256 MiB read",
                        "launch": "one CUDA graph per step (per-call times from a second graph with events between calls)",
+                       "soak_steps": soak_steps,
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": steps * sum(c["launches"] for c in calls), "clocks": clocks,

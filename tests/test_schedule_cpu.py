@@ -1,9 +1,10 @@
 """The prefill kernel's schedule, read through the C ABI without a GPU
 (attn_fwd_prefill_visits), checked against first principles.
 
-FlashAttention-2 ("Parallelism", "Work partitioning"): the output splits into
-independent query tiles, and each walks the K/V tiles that hold at least one
-unmasked key of its rows.  Under the causal mask (bottom-right aligned when
+Lab 02, "La estructura del kernel" (one program per batch x head and query
+tile) and the cruxr.ai "FlashAttention" loop (outer over Q blocks, inner over
+K/V blocks): the output splits into independent query tiles, and each walks
+the K/V tiles that hold at least one unmasked key of its rows.  Under the causal mask (bottom-right aligned when
 Nq < Nk) and the sliding window, a K/V tile whose every key is masked for
 every row of the tile adds nothing and is skipped.  So, whatever the item
 shape, the launch must compute every (head, query tile, live K/V tile)
