@@ -178,10 +178,11 @@ int attn_fwd_prefill_visits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int c
  * request has a page table listing the pages that hold its tokens in order,
  * and the attention kernel follows the table instead of reading a flat K and
  * V).  Same result as attn_fwd_ex on each request's K and V gathered into
- * order, with that request's own key count.  Runs the split-KV kernel, so it
- * serves GQA groups of at most 32 query rows ((Hq / Hkv) * Nq <= 32: a
- * decode step, or a few speculative tokens); larger groups return
- * ATTN_ERR_UNSUPPORTED.
+ * order, with that request's own key count.  GQA groups of at most 32 query
+ * rows ((Hq / Hkv) * Nq <= 32: a decode step, or a few speculative tokens)
+ * run the split-KV kernel; larger groups (a prefill, or chunks of one,
+ * against a paged cache) run the tiled tcgen05 prefill kernel, whose TMA
+ * producer follows the page table, one copy per page.
  *
  * Q (DEVICE, B x Hq x Nq x d), O (DEVICE, same), LSE (DEVICE fp32, B x Hq x
  *   Nq, or NULL): as attn_fwd_ex.  Query row i of request b sits at key
@@ -198,9 +199,10 @@ int attn_fwd_prefill_visits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int c
  *   request's length may hold anything (NaN included): they are not used.
  * page_size: a power of two from 8 to 256.  max_pages_per_seq * page_size
  *   must cover max_seq_len; num_pages * Hkv must stay below 2^31 - 1.
- * workspace (DEVICE, 16-byte aligned, required): at least
+ * workspace (DEVICE, 16-byte aligned): at least
  *   attn_fwd_paged_workspace_bytes(...) bytes, not used by an overlapping
- *   call.
+ *   call; required by the split-KV path, not used (may be NULL) by the
+ *   prefill path, whose workspace size is 0.
  * The host checks everything it can see; a page index outside [0,
  * num_pages) or a length out of range is found by the kernel, which reads
  * zeros for that page (or clamps the length), finishes the call and records
@@ -214,13 +216,14 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
 
 /* Workspace bytes attn_fwd_paged wants for these sizes on the current device
  * (the split-KV scratch for max_seq_len keys); 0 when the sizes are invalid
- * or the query group is too large for the split-KV kernel. */
+ * or the call takes the prefill path (query groups of more than 32 rows). */
 size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
 
 /* The path attn_fwd_paged takes for these sizes on the current device:
  * ATTN_PATH_SPLIT_KV_FUSED (each group's last CTA to finish merges the
- * chunks: one launch) or ATTN_PATH_SPLIT_KV (a second, merge kernel); -1 when the
- * sizes are invalid or the query group is too large.  The paged plan caps
+ * chunks: one launch), ATTN_PATH_SPLIT_KV (a second, merge kernel), or
+ * ATTN_PATH_PREFILL (query groups of more than 32 rows: the tiled kernel,
+ * one launch); -1 when the sizes are invalid.  The paged split plan caps
  * the keys per chunk, since request lengths are known only on the device,
  * so it can split more finely than the flat call of max_seq_len keys.  No
  * device work. */

@@ -145,13 +145,10 @@ def test_bad_length_reported(attn):
 
 
 def test_host_errors(attn):
-    """Group too large for the split-KV kernel; workspace too small."""
+    """Workspace too small for the split-KV path (a group too large for it
+    takes the prefill path instead: tests/test_paged_prefill_gpu.py)."""
     dev = torch.device("cuda:0")
-    shape = ai.PagedShape(1, 8, 1, 8, 256, 64, 16, "fp16", True, 0, None, (256,), 1, 0)
-    q, k, v, table, lens = ai.make_paged(shape, 108, 0)
-    with pytest.raises(attn.AttnError) as e:
-        attn.flash_attn_paged(q.to(dev), k.to(dev), v.to(dev), table.to(dev), lens.to(dev), 256)
-    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_fwd_paged_path(1, 8, 1, 8, 256, 64) == attn.ATTN_PATH_PREFILL
     shape = ai.PagedShape(1, 8, 1, 2, 256, 64, 16, "fp16", True, 0, None, (256,), 1, 0)
     q, k, v, table, lens = ai.make_paged(shape, 108, 1)
     with pytest.raises(attn.AttnError) as e:
@@ -198,10 +195,10 @@ def test_workload_full_size(attn, oracle_mod, idx):
 def test_paged_plan(attn):
     """The paged plan caps the keys per chunk (lengths are known only on the
     device): the ragged benchmark call keeps the fused merge, the group too
-    large for the split-KV kernel has no paged path, and a full-length call
+    large for the split-KV kernel takes the prefill path, and a full-length call
     that already splits finely plans like the flat call."""
     assert attn.attn_fwd_paged_path(32, 32, 8, 1, 8192, 128) == attn.ATTN_PATH_SPLIT_KV_FUSED
-    assert attn.attn_fwd_paged_path(1, 8, 1, 8, 256, 64) == -1
+    assert attn.attn_fwd_paged_path(1, 8, 1, 8, 256, 64) == attn.ATTN_PATH_PREFILL
     assert attn.attn_fwd_paged_path(4, 32, 8, 1, 8192, 128) == attn.attn_fwd_path(4, 32, 8, 1, 8192, 128, True)
     assert attn.attn_fwd_paged_workspace_bytes(4, 32, 8, 1, 8192, 128) == \
         attn.attn_fwd_workspace_bytes(4, 32, 8, 1, 8192, 128)

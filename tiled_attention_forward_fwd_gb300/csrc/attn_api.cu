@@ -157,18 +157,20 @@ static std::atomic<unsigned> g_split_token{0};
 // register split (setmaxnreg) is sized for: kThreads x kLaunchRegs
 // registers; any other allocation could stall.
 template <int D, bool BF16>
-static void (*prefill_kernel(int sched))(FwdParams) {
+static void (*prefill_kernel(int sched, bool paged))(FwdParams) {
+  if (paged) return sched == kSchedHalves ? attn_fwd_kernel<D, BF16, kSchedHalves, true>
+                                          : attn_fwd_kernel<D, BF16, kSchedPlain, true>;
   return sched == kSchedSplit    ? attn_fwd_kernel<D, BF16, kSchedSplit>
          : sched == kSchedHalves ? attn_fwd_kernel<D, BF16, kSchedHalves>
                                  : attn_fwd_kernel<D, BF16, kSchedPlain>;
 }
 
 template <int D, bool BF16>
-static bool prefill_kernel_ready(int dev, int sched) {
-  static std::once_flag once[3][64];
-  static bool ok[3][64];
-  auto kern = prefill_kernel<D, BF16>(sched);
-  const int k = sched;
+static bool prefill_kernel_ready(int dev, int sched, bool paged = false) {
+  static std::once_flag once[5][64];
+  static bool ok[5][64];
+  auto kern = prefill_kernel<D, BF16>(sched, paged);
+  const int k = paged ? (sched == kSchedHalves ? 4 : 3) : sched;  // one slot per kernel
   std::call_once(once[k][dev], [&] {
     cudaFuncAttributes fa;
     ok[k][dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -211,7 +213,7 @@ static bool prefill_schedule(const Shape &s, bool split, int sms_now, FwdParams 
     // tiles, the two softmax warpgroups split them, so that no warpgroup
     // idles while a long tile runs; shorter ones do not repay the merge.
     int beg = 0, end = 0;
-    tile_range(p, static_cast<int>((ntiles - 1) * kBM), beg, end);
+    tile_range(p, static_cast<int>((ntiles - 1) * kBM), p.Nk, beg, end);
     p.pair_mode = (end - beg >= 4) ? kPairHalves : kPairSingle;
     p.n_row_blocks = static_cast<int>(ntiles);
   } else {
@@ -255,24 +257,53 @@ static bool prefill_schedule(const Shape &s, bool split, int sms_now, FwdParams 
   return true;
 }
 
+// A paged K/V cache: the page pool and, per request, its page table and length.
+struct PagedKV {
+  const int *block_table;
+  const int *seq_lens;
+  int page_size, num_pages, max_pages;
+};
+
+static int log2_pow2(int x) {
+  int sh = 0;
+  while ((1 << sh) < x) ++sh;
+  return sh;
+}
+
+// The tiled prefill kernel; with `pg`, on a paged K/V cache (K and V are then
+// the pools, s.Nk the largest request length, and there is no split).
 template <int D, bool BF16>
 static attn_status_t launch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
-                                   const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                                   const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream,
+                                   const PagedKV *pg = nullptr) {
   using Cfg = FwdCfg<D>;
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const long long zq = static_cast<long long>(s.B) * s.Hq;
   const long long zk = static_cast<long long>(s.B) * s.Hkv;
-  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmK, K, D, s.Nk, zk, BF16) ||
-      !make_map(&p.tmV, V, D, s.Nk, zk, BF16) || (Cfg::kStoreOViaSmem && !make_map(&p.tmO, O, D, s.Nq, zq, BF16)))
+  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || (Cfg::kStoreOViaSmem && !make_map(&p.tmO, O, D, s.Nq, zq, BF16)))
     return ATTN_ERR_CUDA;
+  if (pg == nullptr) {
+    if (!make_map(&p.tmK, K, D, s.Nk, zk, BF16) || !make_map(&p.tmV, V, D, s.Nk, zk, BF16)) return ATTN_ERR_CUDA;
+  } else {
+    const long long slabs = static_cast<long long>(pg->num_pages) * s.Hkv;
+    const int box = std::min(pg->page_size, kBN);
+    if (!make_map(&p.tmK, K, D, pg->page_size, slabs, BF16, box) ||
+        !make_map(&p.tmV, V, D, pg->page_size, slabs, BF16, box))
+      return ATTN_ERR_CUDA;
+    p.block_table = pg->block_table;
+    p.seq_lens = pg->seq_lens;
+    p.page_shift = log2_pow2(pg->page_size);
+    p.max_pages = pg->max_pages;
+    p.num_pages = pg->num_pages;
+  }
   int *status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
   p.O = O;
   p.lse = LSE;
   p.status = status;
   const int sms = device_sm_count();
-  const size_t split_bytes = ws ? split_plan_bytes(s, sms) : 0;
+  const size_t split_bytes = (ws && pg == nullptr) ? split_plan_bytes(s, sms) : 0;
   if (split_bytes > 0 && (ws_bytes < split_bytes || !aligned16(ws))) return ATTN_ERR_INVALID_ARG;
   int sched = kSchedPlain, grid = 0;
   if (!prefill_schedule(s, split_bytes > 0, sms, p, sched, grid)) return ATTN_ERR_INVALID_ARG;
@@ -291,10 +322,10 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
   p.timeout_ns = g_timeout_ns.load();
   p.stall_after = g_stall_after.load();
 
-  auto kern = prefill_kernel<D, BF16>(sched);
+  auto kern = prefill_kernel<D, BF16>(sched, pg != nullptr);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (!prefill_kernel_ready<D, BF16>(dev, sched)) return ATTN_ERR_UNSUPPORTED;
+  if (!prefill_kernel_ready<D, BF16>(dev, sched, pg != nullptr)) return ATTN_ERR_UNSUPPORTED;
   if (grid <= 0) return ATTN_ERR_CUDA;
   if (launch_pdl(kern, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -302,12 +333,13 @@ static attn_status_t launch_prefill(const void *Q, const void *K, const void *V,
 }
 
 static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
-                                      const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                                      const Shape &s, void *ws, size_t ws_bytes, cudaStream_t stream,
+                                      const PagedKV *pg = nullptr) {
   const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
-  if (s.d == 64) return bf16 ? launch_prefill<64, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream)
-                             : launch_prefill<64, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream);
-  return bf16 ? launch_prefill<128, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream)
-              : launch_prefill<128, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream);
+  if (s.d == 64) return bf16 ? launch_prefill<64, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg)
+                             : launch_prefill<64, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg);
+  return bf16 ? launch_prefill<128, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg)
+              : launch_prefill<128, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg);
 }
 
 // ---------------------------------------------------------------- split-KV (decode) path
@@ -413,13 +445,6 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   return decode_plan(B, Hq, Hkv, Nq, Nk, d).bytes;
 }
 
-
-// A paged K/V cache: the page pool and, per request, its page table and length.
-struct PagedKV {
-  const int *block_table;
-  const int *seq_lens;
-  int page_size, num_pages, max_pages;
-};
 
 template <int D, bool BF16>
 static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
@@ -673,17 +698,21 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
   // copy coordinates are 32-bit: the pool's slabs and one past them
   if (static_cast<long long>(num_pages) * Hkv >= 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
-  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
-  if (pl.bytes == 0) return ATTN_ERR_UNSUPPORTED;
-  if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   const PagedKV pg{block_table, seq_lens, page_size, num_pages, max_pages_per_seq};
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
+  if (pl.bytes == 0) {
+    // groups of more than 32 query rows: the tiled prefill kernel on the pages
+    if (static_cast<long long>(B) * Hq * ((Nq + kBM - 1) / kBM) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    return dispatch_prefill(Q, K_pages, V_pages, O, LSE, s, nullptr, 0, stream, &pg);
+  }
+  if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   return dispatch_decode(Q, K_pages, V_pages, O, LSE, s, pl, static_cast<float *>(workspace), stream, &pg);
 }
 
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || max_seq_len <= 0 || (d != 64 && d != 128) || Hq % Hkv) return -1;
   const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
-  if (pl.bytes == 0) return -1;
+  if (pl.bytes == 0) return ATTN_PATH_PREFILL;  // larger query groups: the tiled prefill kernel
   return pl.fused ? ATTN_PATH_SPLIT_KV_FUSED : ATTN_PATH_SPLIT_KV;
 }
 

@@ -59,7 +59,7 @@ constexpr int kDecMaxRows = 32;  // query rows of one group handled by one CTA
 constexpr int kDecMaxChunks = 1024;  // key chunks per group (bounds the merge kernel's shared memory)
 constexpr int kDecFusedMerge = 8192;  // rows x chunks x d of a group merged by the split kernel itself
 
-enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecBadIndex = 0x203 };
+enum DecodeError : int { kErrDecWaitKV = 0x201, kErrDecBadIndex = kErrDeviceArg };
 
 struct DecParams {
   // flat: (d, Nk, B*Hkv), box 64 x 64 x 1; paged: (d, page_size,

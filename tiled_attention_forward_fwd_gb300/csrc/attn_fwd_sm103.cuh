@@ -88,6 +88,16 @@ struct FwdParams {
   float2 *ws_ml;      // [CTA][tile][128 rows]
   unsigned *ws_flag;  // [CTA][tile]
   int2 split_at[kMaxSplitCtas + 1];
+  // Paged K/V (the kPaged kernels; the motivation page's "PagedAttention es
+  // un problema distinto"): token t of request b sits in pool page
+  // block_table[b * max_pages + t / page_size], slot t % page_size; request b
+  // holds seq_lens[b] keys (read on the device; Nk is the largest), and its
+  // query rows are its last Nq positions.  tmK / tmV view the pools as (d,
+  // page_size, num_pages * Hkv) with boxes of min(page_size, 128) rows.
+  const int *block_table;
+  const int *seq_lens;
+  int page_shift;  // log2(page_size), 3..8
+  int max_pages, num_pages;
 };
 
 template <int D>
@@ -180,13 +190,15 @@ struct Item {
   int obeg[2], oend[2];  // live K/V tile range of each tile in the whole item
   int iubeg, iuend;      // union range of the whole item
   int item;
+  int nk;                // keys of the item's request (Nk unless paged)
 };
 
-ATTN_HD void tile_range(const FwdParams &p, int row0, int &beg, int &end) {
+// Live K/V tiles [beg, end) of the query tile at row0 of a request with nk keys.
+ATTN_HD void tile_range(const FwdParams &p, int row0, int nk, int &beg, int &end) {
   const int i1 = min(row0 + kBM, p.Nq);
-  const int off = p.Nk - p.Nq;
+  const int off = nk - p.Nq;
   const int p0 = row0 + off, p1 = i1 - 1 + off;
-  const int nkt = (p.Nk + kBN - 1) / kBN;
+  const int nkt = (nk + kBN - 1) / kBN;
   beg = 0;
   end = nkt;
   if (p.causal) {
@@ -209,12 +221,33 @@ ATTN_HD void tile_range(const FwdParams &p, int row0, int &beg, int &end) {
 //                softmax warpgroups work on every item (few, longer tiles)
 enum PairMode : int { kPairRows = 0, kPairHeads = 1, kPairSingle = 2, kPairHalves = 3 };
 
+#ifdef __CUDACC__
+// Keys of paged request b, read on the device: a length out of range (below
+// Nq when causal, below 1, above the largest) is recorded and clamped.
+__device__ __forceinline__ int request_keys(const FwdParams &p, int b) {
+  int len = __ldg(p.seq_lens + b);
+  const int lo = p.causal ? p.Nq : 1;
+  if (len < lo || len > p.Nk) {
+    atomicCAS(p.status, 0, kErrDeviceArg);
+    len = min(max(len, lo), p.Nk);
+  }
+  return len;
+}
+#endif
+
+template <bool kPaged = false>
 ATTN_HD Item decode_item(const FwdParams &p, int item) {
   Item it;
   it.item = item;
   int idx, slot, hs;
   fastdiv_divmod(p.fd_slots, item, idx, slot);  // idx: longest items first
   fastdiv_divmod(p.fd_heads, slot, it.b, hs);
+  it.nk = p.Nk;
+  if constexpr (kPaged) {
+#ifdef __CUDA_ARCH__
+    it.nk = request_keys(p, it.b);
+#endif
+  }
   if (p.pair_mode == kPairHeads) {
     const int rb = p.n_row_blocks - 1 - idx;
     const int h0 = hs * 2;
@@ -243,7 +276,7 @@ ATTN_HD Item decode_item(const FwdParams &p, int item) {
     it.exists[t] = it.valid[t];
     it.beg[t] = it.end[t] = 0;
     if (it.valid[t]) {
-      tile_range(p, it.row0[t], it.beg[t], it.end[t]);
+      tile_range(p, it.row0[t], it.nk, it.beg[t], it.end[t]);
       it.ubeg = it.ubeg < it.beg[t] ? it.ubeg : it.beg[t];
       it.uend = it.uend > it.end[t] ? it.uend : it.end[t];
     }
@@ -314,17 +347,17 @@ ATTN_HD int num_pieces(const FwdParams &p, int c, int g) {
 
 // The k-th piece of the work of CTA c of g; false when there is none (the
 // last pass over the item list may be short).
-template <bool kSplit>
+template <bool kSplit, bool kPaged = false>
 ATTN_HD bool piece_at(const FwdParams &p, int c, int g, int k, Item &it) {
   if constexpr (!kSplit) {
     const int item = item_of(k, c, g);
     if (item >= p.n_items) return false;
-    it = decode_item(p, item);
+    it = decode_item<kPaged>(p, item);
     return true;
   }
   const int2 s = p.split_at[c], e = p.split_at[c + 1];
   const int item = s.x + k;
-  it = decode_item(p, item);
+  it = decode_item<kPaged>(p, item);
   clip_item(it, k == 0 ? s.y : 0, item == e.x ? e.y : (1 << 30));
   return true;
 }
@@ -387,7 +420,7 @@ constexpr uint32_t kBarHalfReady = 7, kBarHalfRead = 8, kBarHalvesThreads = 256;
 // the others' code.
 enum Sched : int { kSchedPlain = 0, kSchedSplit = 1, kSchedHalves = 2 };
 
-template <int D, bool BF16, int kSched>
+template <int D, bool BF16, int kSched, bool kPaged = false>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool kSplit = kSched == kSchedSplit;
   constexpr bool kHalves = kSched == kSchedHalves;
@@ -468,7 +501,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       const int npieces = num_pieces<kSplit>(p, blockIdx.x, gridDim.x);
       for (int pk = 0; ok && pk < npieces; ++pk) {
         Item it;
-        if (!piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, it)) continue;
+        if (!piece_at<kSplit, kPaged>(p, blockIdx.x, gridDim.x, pk, it)) continue;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || !it.valid[t]) continue;
@@ -499,16 +532,48 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
             ok = false;
             break;
           }
-          if (elect_one()) {
-            mbar_arrive_expect_tx(bKVfull(s), 2 * C::kTileBytes);
+          if constexpr (!kPaged) {
+            if (elect_one()) {
+              mbar_arrive_expect_tx(bKVfull(s), 2 * C::kTileBytes);
 #pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc)
-              tma_load_3d(sK + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmK, bKVfull(s), cc * 64, j * kBN, zkv);
+              for (int cc = 0; cc < D / 64; ++cc)
+                tma_load_3d(sK + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmK, bKVfull(s), cc * 64, j * kBN, zkv);
 #pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc)
-              tma_load_3d(sV + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmV, bKVfull(s), cc * 64, j * kBN, zkv);
+              for (int cc = 0; cc < D / 64; ++cc)
+                tma_load_3d(sV + s * C::kTileBytes + cc * C::kBoxBytes, &p.tmV, bKVfull(s), cc * 64, j * kBN, zkv);
+            }
+            __syncwarp();
+          } else {
+            // The tile's keys [j * 128, +128) lie in 128 / page_size pages
+            // (or in part of one page).  Lane l holds the pool slab (page *
+            // Hkv + kv head) of the l-th page and copies its box; a page past
+            // the request's end, or an index outside the pool (recorded),
+            // becomes the slab one past the pool, which reads as zeros.
+            const int sh = p.page_shift;
+            const int npg = sh < 7 ? (kBN >> sh) : 1;
+            const int lp = ((j * kBN) >> sh) + lane;  // logical page of lane l
+            int slab = p.num_pages * p.Hkv;
+            if (lane < npg && lp < ((it.nk + (1 << sh) - 1) >> sh)) {
+              const int page = __ldg(p.block_table + static_cast<size_t>(it.b) * p.max_pages + lp);
+              if (page >= 0 && page < p.num_pages)
+                slab = page * p.Hkv + it.kvh;
+              else
+                atomicCAS(p.status, 0, kErrDeviceArg);
+            }
+            const int y = sh < 7 ? 0 : (j * kBN) & ((1 << sh) - 1);  // first row within the page
+            const uint32_t off = sh < 7 ? static_cast<uint32_t>(lane << sh) * 128u : 0u;
+            if (elect_one()) mbar_arrive_expect_tx(bKVfull(s), 2 * C::kTileBytes);
+            __syncwarp();
+            if (lane < npg) {
+#pragma unroll
+              for (int cc = 0; cc < D / 64; ++cc)
+                tma_load_3d(sK + s * C::kTileBytes + cc * C::kBoxBytes + off, &p.tmK, bKVfull(s), cc * 64, y, slab);
+#pragma unroll
+              for (int cc = 0; cc < D / 64; ++cc)
+                tma_load_3d(sV + s * C::kTileBytes + cc * C::kBoxBytes + off, &p.tmV, bKVfull(s), cc * 64, y, slab);
+            }
+            __syncwarp();
           }
-          __syncwarp();
           ckv = c + 1;
         }
       }
@@ -539,11 +604,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       int ckv = 0;       // ring slots passed
       int kv_seen = -1;  // last ring slot whose arrival was waited for
       bool ok = true;
-      // the pending P V: (stage, accumulate, last) of the previous step
+      // the pending P V: (stage, accumulate, last) of the previous step, and
+      // (paged) the rows of its V tile that hold the request's keys
       bool pending = false;
       int pv_stage = 0;
       uint32_t pv_acc = 0;
       bool pv_last = false;
+      int pv_valid = kBN;
       auto wait_kv = [&](int c) {
         if (ok && c > kv_seen) {
           ok = mbar_wait_warp(bKVfull(c % NS), (c / NS) & 1, wc, kErrWaitKV);
@@ -591,6 +658,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
           }
           __syncwarp();
         }
+        if (kPaged && ok && pv_valid < kBN) {
+          // Paged: the slots of the request's last page past its end hold
+          // whatever the pool held (NaN included); their P is 0, but 0 x NaN
+          // is not, so their V rows are zeroed before P V (whole 128-byte
+          // rows: the swizzle permutes chunks within a row).  Rows past the
+          // last page were read as zeros.
+          const int zend = min(kBN, ((pv_valid + (1 << p.page_shift) - 1) >> p.page_shift) << p.page_shift);
+          const uint32_t vbase = sV + pv_stage * C::kTileBytes;
+          for (int r = pv_valid + lane; r < zend; r += 32)
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc)
+#pragma unroll
+              for (int q = 0; q < 8; ++q) st_shared_v4(vbase + cc * C::kBoxBytes + r * 128 + q * 16, 0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();  // the zeros are visible to the tensor core
+          __syncwarp();
+        }
         if (ok) {
           tc_fence_after();
           const uint64_t vd = sdesc_sw128(sV + pv_stage * C::kTileBytes, C::kBoxBytes, 1024);
@@ -607,7 +690,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       const int npieces = num_pieces<kSplit>(p, blockIdx.x, gridDim.x);
       for (int pk = 0; pk < npieces; ++pk) {
         Item it;
-        if (!piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, it)) continue;
+        if (!piece_at<kSplit, kPaged>(p, blockIdx.x, gridDim.x, pk, it)) continue;
         const bool tvalid = t ? it.valid[1] : it.valid[0];
         const int tbeg = tvalid ? (t ? it.beg[1] : it.beg[0]) : it.uend;
         const int tend = tvalid ? (t ? it.end[1] : it.end[0]) : it.uend;
@@ -644,6 +727,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
             pv_stage = c % NS;
             pv_acc = (j > tbeg) ? 1u : 0u;
             pv_last = (j + 1 == tend);
+            if constexpr (kPaged) pv_valid = min(kBN, it.nk - j * kBN);
           }
           // The item's last P V goes out now: it releases a K/V stage that a
           // later fill (and this warp's next waits) may need.
@@ -692,7 +776,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
     const int npieces = num_pieces<kSplit>(p, blockIdx.x, gridDim.x);
     for (int pk = 0; pk < npieces; ++pk) {
       Item it;
-      if (!piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, it)) continue;
+      if (!piece_at<kSplit, kPaged>(p, blockIdx.x, gridDim.x, pk, it)) continue;
       // this warpgroup's tile, as scalars (t is not a compile-time index)
       const bool tvalid = t ? it.valid[1] : it.valid[0];
       if (!tvalid) continue;
@@ -700,9 +784,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       const int tbeg = t ? it.beg[1] : it.beg[0];
       const int tend = t ? it.end[1] : it.end[0];
       const int tbh = t ? it.bh[1] : it.bh[0];
-      const int pos = trow0 + row + (p.Nk - p.Nq);  // absolute position of this query row
-      const int p0 = trow0 + (p.Nk - p.Nq);
-      const int p1 = min(trow0 + kBM, p.Nq) - 1 + (p.Nk - p.Nq);
+      const int nk = it.nk;                    // keys of this item's request
+      const int pos = trow0 + row + (nk - p.Nq);  // absolute position of this query row
+      const int p0 = trow0 + (nk - p.Nq);
+      const int p1 = min(trow0 + kBM, p.Nq) - 1 + (nk - p.Nq);
       // kPairHalves with both halves: tile 0 hands its half to tile 1
       const bool half_out = kHalves && t == 0 && it.valid[1];
       const bool half_merge = kHalves && t == 1;
@@ -726,12 +811,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
         }
         {
           const int key0 = j * kBN;
-          const bool need_mask = (key0 + kBN - 1 >= p.Nk) || (p.causal && key0 + kBN - 1 > p0) ||
+          const bool need_mask = (key0 + kBN - 1 >= nk) || (p.causal && key0 + kBN - 1 > p0) ||
                                  (p.window > 0 && key0 <= p1 - p.window);
           if (need_mask) {
             // The row's live keys are one interval: below Nk, not after the
             // row (causal), within the window.  [lo, hi) relative to key0.
-            const int hi = min(p.Nk, p.causal ? pos + 1 : p.Nk) - key0;
+            const int hi = min(nk, p.causal ? pos + 1 : nk) - key0;
             const int lo = (p.window > 0) ? pos - p.window + 1 - key0 : -1;
 #pragma unroll
             for (int cc = 0; cc < kBN; ++cc)
@@ -819,7 +904,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) attn_fwd_kernel(const 
       Item ie{};
       bool part_out = false, merge_in = false;
       if constexpr (kSplit) {
-        piece_at<kSplit>(p, blockIdx.x, gridDim.x, pk, ie);
+        piece_at<kSplit, kPaged>(p, blockIdx.x, gridDim.x, pk, ie);
         part_out = ie.ubeg > ie.iubeg;
         merge_in = ie.ubeg == ie.iubeg && ie.uend < ie.iuend;
       }

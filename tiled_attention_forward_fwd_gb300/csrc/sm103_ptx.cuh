@@ -100,6 +100,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Status code of a kernel that found a device-side argument out of range (a
+// page index outside the pool, a sequence length out of range); the host
+// reports it as ATTN_ERR_DEVICE_ARG.
+constexpr int kErrDeviceArg = 0x203;
+
 // Shared per-CTA abort flag + global status word used by bounded waits.
 struct WaitCtl {
   volatile int *abort_flag;  // shared memory
