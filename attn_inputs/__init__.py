@@ -121,10 +121,24 @@ class AttnShape:
     window: int = 0
     sm_scale: float | None = None
     key_scale: float = 1.0
+    kv_int8: bool = False  # K and V stored as int8 codes with one scale per tensor
 
     @property
     def scale(self) -> float:
         return self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(self.d)
+
+
+def make_qkv_int8(shape: AttnShape, config_id: int = 0, layer: int = 0):
+    """Seeded (Q, K codes, K scale, V codes, V scale): Q in the storage
+    dtype; K and V drawn like make_qkv's (before rounding) and quantised per tensor
+    (quantize_int8)."""
+    q = normal_tensor(seed_for(config_id, layer, "Q"), (shape.B, shape.Hq, shape.Nq, shape.d), shape.dtype)
+    k = normal_tensor(seed_for(config_id, layer, "K"), (shape.B, shape.Hkv, shape.Nk, shape.d), "f64",
+                      scale=shape.key_scale)
+    v = normal_tensor(seed_for(config_id, layer, "V"), (shape.B, shape.Hkv, shape.Nk, shape.d), "f64")
+    kc, ks = quantize_int8(k)
+    vc, vs = quantize_int8(v)
+    return q, kc, ks, vc, vs
 
 
 def make_qkv(shape: AttnShape, config_id: int = 0, layer: int = 0):
@@ -264,6 +278,9 @@ def workload_calls(name: str):
                 (AttnShape(4, 32, 8, 1, 8192, 128, "bf16", True, 0, None), 5, 1)]
     if name == "mha_n64_bw":  # bandwidth-sized sibling of mha_n64: B=512, H=32, N=64, d=64, fp16
         return [(AttnShape(512, 32, 32, 64, 64, 64, "fp16", c, 0, 0.125), 6, int(c)) for c in (False, True)]
+    if name == "mqa_decode_int8":  # mqa_decode's step on an INT8 K/V cache (per-tensor scales)
+        return [(AttnShape(4, 32, 1, 1, 8192, 128, "bf16", True, 0, None, kv_int8=True), 8, 0),
+                (AttnShape(4, 32, 8, 1, 8192, 128, "bf16", True, 0, None, kv_int8=True), 8, 1)]
     if name == "paged_decode":
         # one decode step on a paged cache of 16-token pages, bf16, d=128, GQA 32/8:
         # the mqa_decode Hkv=8 call with every request at 8192 tokens (same
@@ -275,4 +292,4 @@ def workload_calls(name: str):
 
 
 WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw",
-                  "paged_decode"]
+                  "paged_decode", "mqa_decode_int8"]

@@ -49,6 +49,7 @@ WORKLOAD_TEXT = {
     "mha_n64_bw": "MHA forward B=512, H=32, N=64, d=64, fp16, causal in {false,true}",
     "paged_decode": "decode on a paged cache (16-token pages, shuffled pool), Hq=32, Hkv=8, Nq=1, d=128, bf16: "
                     "B=4 at 8192 tokens; B=32 at drawn lengths 512..8192",
+    "mqa_decode_int8": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16 Q, int8 K/V (per-tensor scales)",
 }
 # Device sources of each kernel family: a committed DRAM-traffic figure
 # (profiles/traffic.json) counts only while they hash to the value recorded
@@ -200,7 +201,8 @@ def call_label(s) -> str:
     if isinstance(s, ai.PagedShape):
         return (f"paged_B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_L{s.max_seq_len}_ps{s.page_size}_d{s.d}_{s.dtype}"
                 f"_c{int(s.causal)}_w{s.window}")
-    return (f"B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}_c{int(s.causal)}_w{s.window}")
+    return (f"B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}{'_kv8' if s.kv_int8 else ''}"
+            f"_c{int(s.causal)}_w{s.window}")
 
 
 def prepare_paged(shape, cid, layer, device):
@@ -235,9 +237,14 @@ def prepare(workload: str, device):
         if isinstance(shape, ai.PagedShape):
             calls.append(prepare_paged(shape, cid, layer, device))
             continue
-        q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+        if shape.kv_int8:
+            q, k, ks, v, vs = ai.make_qkv_int8(shape, cid, layer)
+        else:
+            q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
         c = {"shape": shape, "q_host": q, "k_host": k, "v_host": v,
              "q": q.to(device), "k": k.to(device), "v": v.to(device)}
+        if shape.kv_int8:
+            c["k_scale"], c["v_scale"] = ks, vs
         c["o"] = torch.empty_like(c["q"])
         c["lse"] = torch.empty((shape.B, shape.Hq, shape.Nq), device=device, dtype=torch.float32)
         c["dtype_code"] = attn.ATTN_DTYPE_BF16 if shape.dtype == "bf16" else attn.ATTN_DTYPE_FP16
@@ -274,6 +281,14 @@ def launch(c, stream_handle):
                                  stream_handle)
         if st != attn.ATTN_OK:
             raise RuntimeError(f"attn_fwd_paged failed: {attn.attn_status_string(st)}")
+        return
+    if s.kv_int8:
+        st = attn.attn_fwd_kv_int8(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["k_scale"],
+                                   c["v_scale"], c["o"].data_ptr(), c["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq,
+                                   s.Nk, s.d, s.causal, s.window, s.scale, c["dtype_code"], ws.data_ptr(),
+                                   ws.numel(), stream_handle)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_fwd_kv_int8 failed: {attn.attn_status_string(st)}")
         return
     st = attn.attn_fwd_ex(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["o"].data_ptr(),
                           c["lse"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale,
@@ -375,10 +390,12 @@ def e2e_timing(calls, steps, warmup, device, stream):
     need = 0
     for c in calls:
         s = c["shape"]
-        if c.get("paged"):
-            # the paged call's inputs (pools, table, lengths, Q) are copied
-            # into its device tensors, then attn_fwd_paged runs on them
-            ph = {k: c[k + "_host"].pin_memory() for k in ("q", "k", "v", "table", "lens")}
+        if c.get("paged") or s.kv_int8:
+            # the inputs of a paged call (pools, table, lengths, Q) or of an
+            # int8 call (Q, codes) are copied into its device tensors, then
+            # the call runs on them
+            names = ("q", "k", "v", "table", "lens") if c.get("paged") else ("q", "k", "v")
+            ph = {k: c[k + "_host"].pin_memory() for k in names}
             ph["o"] = torch.empty_like(ph["q"]).pin_memory()
             ph["lse"] = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32).pin_memory()
             pinned.append(ph)
@@ -393,7 +410,7 @@ def e2e_timing(calls, steps, warmup, device, stream):
     h2d = d2h = 0
     for c in calls:
         s = c["shape"]
-        h2d += (c["q"].numel() + c["k"].numel() + c["v"].numel()) * 2
+        h2d += c["q"].numel() * 2 + (c["k"].numel() + c["v"].numel()) * c["k"].element_size()
         if c.get("paged"):
             h2d += (c["table"].numel() + c["lens"].numel()) * 4
         d2h += c["o"].numel() * 2 + s.B * s.Hq * s.Nq * 4
@@ -401,9 +418,9 @@ def e2e_timing(calls, steps, warmup, device, stream):
     def one_step():
         for c, ph in zip(calls, pinned):
             s = c["shape"]
-            if c.get("paged"):
+            if c.get("paged") or s.kv_int8:
                 with torch.cuda.stream(stream):
-                    for k in ("q", "k", "v", "table", "lens"):
+                    for k in (("q", "k", "v", "table", "lens") if c.get("paged") else ("q", "k", "v")):
                         c[k].copy_(ph[k], non_blocking=True)
                     launch(c, stream.cuda_stream)
                     ph["o"].copy_(c["o"], non_blocking=True)
@@ -449,7 +466,11 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
             q, k, v, table, lens = ai.make_paged(shape, cid, layer)
             prepared.append((shape, q, k.to(torch.float64), v.to(torch.float64), table, lens))
             continue
-        q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+        if shape.kv_int8:  # the oracle reads the exactly dequantised cache
+            q, kc, ks, vc, vs = ai.make_qkv_int8(shape, cid, layer)
+            k, v = kc.to(torch.float64) * ks, vc.to(torch.float64) * vs
+        else:
+            q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
         prepared.append((shape, q.reshape(-1, shape.d), k.to(torch.float64), v.to(torch.float64)))
 
     def run_paged(shape, q, k, v, table, lens, rows_per_call):

@@ -229,6 +229,27 @@ size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_se
  * device work. */
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
 
+/* Decode over an INT8 K/V cache (cruxr.ai "Optimizaciones de Atencion",
+ * section "Elegir optimizaciones de atencion": INT8 quantisation of the KV
+ * cache is among the optimisations that compose with the others; the page
+ * gives no scheme, so this is the plainest one).  K = k_scale * K_codes and
+ * V = v_scale * V_codes with symmetric int8 codes (-127..127) and one fp32
+ * scale per tensor; otherwise the same result as attn_fwd_ex on the
+ * dequantised K and V.  The kernel loads the codes (half the bytes of a
+ * 16-bit cache), widens them exactly to the dtype of Q, folds k_scale into
+ * the softmax scale and v_scale into O.
+ *
+ * K_codes, V_codes (DEVICE, int8, B x Hkv x Nk x d, dense, 16-byte aligned);
+ *   every other argument as attn_fwd_ex.  Only shapes that take the split-KV
+ *   path (query groups of at most 32 rows: (Hq / Hkv) * Nq <= 32) are served;
+ *   others return ATTN_ERR_UNSUPPORTED.  workspace (DEVICE, required): at
+ *   least attn_fwd_workspace_bytes(...) bytes, as for attn_fwd_ex.
+ *   k_scale, v_scale: finite and > 0, else ATTN_ERR_INVALID_ARG. */
+attn_status_t attn_fwd_kv_int8(const void *Q, const void *K_codes, const void *V_codes, float k_scale,
+                               float v_scale, void *O, float *LSE, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                               int causal, int window, float sm_scale, attn_dtype_t dtype, void *workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.

@@ -37,12 +37,12 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     tr = terminalreporter
     tr.section("parity against the stated bound")
     tr.write_line(f"{'config / call':58s} {'dtype':5s} {'max|dO|':>9s} {'stated':>7s} {'over':>6s} {'of':>9s} "
-                  f"{'ulps':>5s} {'max|dLSE|':>9s}  bound")
+                  f"{'ulps':>5s} {'max|dLSE|':>9s}  bound   (ulps: vs the rounded oracle, at |O| >= 1/16)")
     for r in recs:
         if not r["config"]:
             continue
         tr.write_line(f"{r['config'][:58]:58s} {r['dtype']:5s} {r['max_abs_O']:9.2e} {r['stated_tol_O']:7.0e} "
-                      f"{r['n_over_stated']:6d} {r['n_elems']:9d} {r['ulps_to_rounded_oracle']:5d} "
+                      f"{r['n_over_stated']:6d} {r['n_elems']:9d} {r['ulps_to_rounded_oracle']:5.1f} "
                       f"{r.get('max_abs_LSE', float('nan')):9.2e}  {r['bound']}")
         for i, e, a in r["over_stated"]:
             tr.write_line(f"    element {i}: |dO| {e:.3e}, |O_oracle| {a:.3f}")

@@ -83,17 +83,18 @@ RECORDS: list[dict] = []
 MAX_LISTED = 16  # elements over the stated bound listed per comparison
 
 
-def ulps_to_rounded(dtype: str, o: np.ndarray, o_ref: np.ndarray) -> int:
-    """max distance, in steps of the 16-bit output grid, between O_gpu (a
-    16-bit value) and the oracle rounded to the output dtype (RNE, torch):
-    0 where the kernel returned the correctly rounded result."""
+def ulps_to_rounded(dtype: str, o: np.ndarray, o_ref: np.ndarray) -> float:
+    """max |O_gpu - round_dtype(O_oracle)| in ulps of the output grid at the
+    rounded oracle value, over the elements with |O_oracle| >= 1/16 (where the
+    16-bit grid, not the absolute bound, is what limits the error; 0 when
+    there are none): 0 where the kernel returned the correctly rounded
+    result."""
     tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
-
-    def order(x):  # 16-bit patterns -> integers in the order of the values
-        b = torch.from_numpy(np.ascontiguousarray(x)).to(tdt).view(torch.int16).to(torch.int32)
-        return torch.where(b < 0, -(b & 0x7FFF), b)
-
-    return int((order(o) - order(o_ref)).abs().max())
+    r = torch.from_numpy(np.ascontiguousarray(o_ref)).to(tdt).to(torch.float64).numpy()
+    big = np.abs(o_ref) >= 0.0625
+    if not big.any():
+        return 0.0
+    return float((np.abs(o - r)[big] / dtype_ulp(dtype, r[big])).max())
 
 
 def compare(dtype, o, o_ref, lse, lse_ref, label="", a_ref=None, config=None, strict=False):

@@ -36,7 +36,7 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
-            "attn_fwd_decode_plan", "attn_set_test_stall"]
+            "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8"]
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.attn_set_wait_timeout_ns.restype = None
         L.attn_set_test_stall.argtypes = [ci]
         L.attn_set_test_stall.restype = None
+        L.attn_fwd_kv_int8.argtypes = [vp, vp, vp, cf, cf, vp, vp] + [ci] * 8 + [cf, ci, vp, sz, vp]
+        L.attn_fwd_kv_int8.restype = ci
         L.attn_status_string.argtypes = [ci]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_abi_version.argtypes = []
@@ -152,6 +154,13 @@ def attn_fwd_paged(Q, K_pages, V_pages, block_table, seq_lens, O, LSE, B, Hq, Hk
     return lib().attn_fwd_paged(Q, K_pages, V_pages, block_table, seq_lens, O, LSE, B, Hq, Hkv, Nq, max_seq_len, d,
                                 page_size, num_pages, max_pages_per_seq, int(causal), int(window), float(sm_scale),
                                 int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_fwd_kv_int8(Q, K_codes, V_codes, k_scale, v_scale, O, LSE, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale,
+                     dtype, workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_kv_int8(Q, K_codes, V_codes, float(k_scale), float(v_scale), O, LSE, B, Hq, Hkv, Nq, Nk, d,
+                                  int(causal), int(window), float(sm_scale), int(dtype), workspace,
+                                  int(workspace_bytes), stream)
 
 
 def attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d) -> int:
@@ -303,9 +312,46 @@ def flash_attn_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: in
     return out, (lse if return_lse else None)
 
 
+def flash_attn_kv_int8(q, k_codes, v_codes, k_scale: float, v_scale: float, causal: bool = True, window: int = 0,
+                      sm_scale: float | None = None, return_lse: bool = True, out=None, lse=None, workspace=None):
+    """Decode over an INT8 K/V cache (see attn_fwd_kv_int8 in include/attn.h):
+    K = k_scale * k_codes, V = v_scale * v_codes.  q: (B, Hq, Nq, d) fp16 or
+    bf16; k_codes, v_codes: (B, Hkv, Nk, d) int8, on q's device.
+    ``workspace`` (a CUDA byte tensor of at least ``attn_fwd_workspace_bytes``
+    bytes) is allocated when not given.  Returns ``(O, LSE)``.  Runs on the
+    current stream."""
+    torch = _torch()
+    if not (q.is_cuda and k_codes.is_cuda and v_codes.is_cuda):
+        raise ValueError("flash_attn_kv_int8 needs CUDA tensors (no CPU path)")
+    if k_codes.dtype != torch.int8 or v_codes.dtype != torch.int8:
+        raise TypeError("k_codes and v_codes must be int8")
+    if q.dim() != 4 or k_codes.dim() != 4 or k_codes.shape != v_codes.shape:
+        raise ValueError("q must be (B,Hq,Nq,d) and the codes (B,Hkv,Nk,d)")
+    q, k_codes, v_codes = q.contiguous(), k_codes.contiguous(), v_codes.contiguous()
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k_codes.shape[1], k_codes.shape[2]
+    if k_codes.shape[0] != B or k_codes.shape[3] != d:
+        raise ValueError("codes batch / head dim do not match q")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    if workspace is None:
+        need = attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = attn_fwd_kv_int8(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(), k_scale, v_scale, out.data_ptr(),
+                          lse.data_ptr() if return_lse else None, B, Hq, Hkv, Nq, Nk, d, causal, window, scale,
+                          _dtype_code(q), workspace.data_ptr(), workspace.numel(), _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_kv_int8")
+    return out, (lse if return_lse else None)
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and read/clear the kernel status word."""
     return attn_device_status(_stream_handle(device))
 
 
-__all__ = EXPORTED + ["flash_attn_forward", "flash_attn_paged", "device_status", "lib", "AttnError"]
+__all__ = EXPORTED + ["flash_attn_forward", "flash_attn_paged", "flash_attn_kv_int8", "device_status", "lib",
+                      "AttnError"]

@@ -63,6 +63,9 @@ def shape_flops(s, exact: bool = False) -> float:
 
 
 def shape_bytes(s, with_lse: bool = True) -> int:
+    if getattr(s, "kv_int8", False):  # Q and O 16-bit, K and V one byte per element
+        b = 2 * s.d * 2 * s.B * s.Hq * s.Nq + s.d * 2 * s.B * s.Hkv * s.Nk
+        return b + (4 * s.B * s.Hq * s.Nq if with_lse else 0)
     return compulsory_bytes(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, 2, with_lse)
 
 

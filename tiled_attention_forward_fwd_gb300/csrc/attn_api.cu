@@ -59,6 +59,22 @@ static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view (d, rows, slabs) of a dense (slabs, rows, d) int8 tensor, box d x
+// 64 x 1 without swizzle (the decode kernel widens rows itself).
+static bool make_map_s8(CUtensorMap *m, const void *ptr, int d, int rows, long long slabs) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slabs)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(d) * rows};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel on the stream finishes; it waits (griddepcontrol.wait)
 // before touching global memory.
@@ -364,6 +380,8 @@ static int decode_ctas_per_sm_t() {
     for (auto k : {attn_decode_kernel<D, true, RB, false>, attn_decode_kernel<D, false, RB, false>,
                    attn_decode_kernel<D, true, RB, true>, attn_decode_kernel<D, false, RB, true>})
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    for (auto k : {attn_decode_kernel<D, true, RB, false, true>, attn_decode_kernel<D, false, RB, false, true>})
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D, RB, true>::kSmemBytes);
     // flat and paged kernels: the smaller residency (the plan sizes one wave)
     int n = 0, n_paged = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<D, true, RB, false>, kDecThreads,
@@ -446,14 +464,21 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
 }
 
 
+// Scales of an int8 K/V cache (K = k_scale * codes, V = v_scale * codes).
+struct QuantKV {
+  float k_scale, v_scale;
+};
+
 template <int D, bool BF16>
 static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                      const Shape &s, const DecPlan &pl, float *ws, int *status,
-                                     const PagedKV *pg, cudaStream_t stream) {
+                                     const PagedKV *pg, cudaStream_t stream, const QuantKV *qk = nullptr) {
   DecParams p;
   std::memset(&p, 0, sizeof(p));
   const long long zk = static_cast<long long>(s.B) * s.Hkv;
-  if (pg == nullptr) {
+  if (qk != nullptr) {
+    if (!make_map_s8(&p.tmK, K, D, s.Nk, zk) || !make_map_s8(&p.tmV, V, D, s.Nk, zk)) return ATTN_ERR_CUDA;
+  } else if (pg == nullptr) {
     if (!make_map(&p.tmK, K, D, s.Nk, zk, BF16, kDecKeys) || !make_map(&p.tmV, V, D, s.Nk, zk, BF16, kDecKeys))
       return ATTN_ERR_CUDA;
   } else {
@@ -489,7 +514,10 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   // of the first query row
   p.kv_lo = (s.causal && s.window > 0) ? std::max(0, (s.Nk - s.Nq) - s.window + 1) : 0;
   p.kv_hi = s.Nk;
-  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  // the key scale folds into the softmax scale, the value scale into each chunk's O
+  const double ks = qk ? static_cast<double>(qk->k_scale) : 1.0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * ks * 1.4426950408889634074);
+  p.v_scale = qk ? qk->v_scale : 1.f;
   p.timeout_ns = g_timeout_ns.load();
   p.stall_after = g_stall_after.load();
   if (pl.fused) {
@@ -506,7 +534,11 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
   dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(zk));
   const dim3 block(kDecThreads);
   cudaError_t le;
-  if (pg == nullptr)
+  if (qk != nullptr)
+    le = (p.R <= 16)
+             ? launch_pdl(attn_decode_kernel<D, BF16, 1, false, true>, grid, block, DecCfg<D, 1, true>::kSmemBytes, stream, p)
+             : launch_pdl(attn_decode_kernel<D, BF16, 2, false, true>, grid, block, DecCfg<D, 2, true>::kSmemBytes, stream, p);
+  else if (pg == nullptr)
     le = (p.R <= 16) ? launch_pdl(attn_decode_kernel<D, BF16, 1, false>, grid, block, DecCfg<D, 1>::kSmemBytes, stream, p)
                      : launch_pdl(attn_decode_kernel<D, BF16, 2, false>, grid, block, DecCfg<D, 2>::kSmemBytes, stream, p);
   else
@@ -537,15 +569,15 @@ static attn_status_t launch_decode_t(const void *Q, const void *K, const void *V
 
 static attn_status_t dispatch_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                      const Shape &s, const DecPlan &pl, float *ws, cudaStream_t stream,
-                                     const PagedKV *pg = nullptr) {
+                                     const PagedKV *pg = nullptr, const QuantKV *qk = nullptr) {
   int *status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
   const bool bf16 = s.dtype == ATTN_DTYPE_BF16;
   if (s.d == 64)
-    return bf16 ? launch_decode_t<64, true>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream)
-                : launch_decode_t<64, false>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream);
-  return bf16 ? launch_decode_t<128, true>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream)
-              : launch_decode_t<128, false>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream);
+    return bf16 ? launch_decode_t<64, true>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream, qk)
+                : launch_decode_t<64, false>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream, qk);
+  return bf16 ? launch_decode_t<128, true>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream, qk)
+              : launch_decode_t<128, false>(Q, K, V, O, LSE, s, pl, ws, status, pg, stream, qk);
 }
 
 // ---------------------------------------------------------------- short keys (Nk <= 128)
@@ -707,6 +739,23 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
   }
   if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   return dispatch_decode(Q, K_pages, V_pages, O, LSE, s, pl, static_cast<float *>(workspace), stream, &pg);
+}
+
+attn_status_t attn_fwd_kv_int8(const void *Q, const void *K_codes, const void *V_codes, float k_scale,
+                               float v_scale, void *O, float *LSE, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                               int causal, int window, float sm_scale, attn_dtype_t dtype, void *workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  Shape s{B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype};
+  attn_status_t st = validate(Q, K_codes, V_codes, O, LSE, s);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(k_scale) || !(k_scale > 0.f) || !std::isfinite(v_scale) || !(v_scale > 0.f))
+    return ATTN_ERR_INVALID_ARG;
+  if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, Nk, d);
+  if (pl.bytes == 0) return ATTN_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  const QuantKV qk{k_scale, v_scale};
+  return dispatch_decode(Q, K_codes, V_codes, O, LSE, s, pl, static_cast<float *>(workspace), stream, nullptr, &qk);
 }
 
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {

@@ -82,7 +82,8 @@ struct DecParams {
   int causal, window;
   int nchunks, chunk_keys;
   int kv_lo, kv_hi;  // keys any row of a group can see
-  float scale_log2;  // sm_scale * log2(e)
+  float scale_log2;  // sm_scale * log2(e) (int8 K/V: times the key scale)
+  float v_scale;     // int8 K/V: the value scale, applied to each chunk's O (1 otherwise)
   unsigned long long timeout_ns;
   int stall_after;  // test hook: the producer stops after this many K/V tiles (-1: never)
   // paged K/V: token t of request b sits in page block_table[b * max_pages +
@@ -100,23 +101,30 @@ struct DecParams {
 // rows; 6 stages x 1 CTA for 32 rows at d = 128 (whose per-thread O state
 // does not fit two CTAs' registers without spilling); 6 stages x 2 CTAs at
 // d = 64.
-template <int D, int RB>
+// int8 K/V (kQuant): the ring holds tiles of half the bytes, 4 stages (7 at
+// d = 128 with 32 rows, 6 at d = 64), and each warp widens its 16 rows of
+// the current K and V tile into a 16-bit staging tile (same layout as a
+// 16-bit ring tile), so the rest of the kernel is unchanged.
+template <int D, int RB, bool kQuant = false>
 struct DecCfg {
-  static constexpr int kStages = (D == 128 && RB == 1) ? 3 : 6;
+  static constexpr int kStages = kQuant ? (D == 64 ? 6 : (RB == 2 ? 7 : 4)) : ((D == 128 && RB == 1) ? 3 : 6);
   static constexpr int kMinCtas = (D == 128 && RB == 2) ? 1 : 2;
   static constexpr int kBoxBytes = kDecKeys * 128;          // 64 rows x 128 B
-  static constexpr int kTileBytes = kDecKeys * D * 2;       // one K or V tile
+  static constexpr int kTileBytes = kDecKeys * D * 2;       // one 16-bit K or V tile
+  static constexpr int kRingTileBytes = kQuant ? kDecKeys * D : kTileBytes;  // one K or V tile as loaded
   static constexpr int kQBoxBytes = kDecMaxRows * 128;      // 32 rows x 128 B
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = ((kDecMaxRows * D * 2 + 1023) / 1024) * 1024;
-  static constexpr int kStageBytes = 2 * kTileBytes;        // K then V
+  static constexpr int kStageBytes = 2 * kRingTileBytes;    // K then V
+  static constexpr int kOffWide = kOffKV + kStages * kStageBytes;  // kQuant: 16-bit K then V staging
+  static constexpr int kWideBytes = kQuant ? 2 * kTileBytes : 0;
   // kfull, vfull, kempty, vempty [stages]; abort flag; the group counter as first read
-  static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffBar = kOffWide + kWideBytes;
   static constexpr int kOffStats = kOffBar + 256;           // float wm[4][32], wl[4][32], rinv[32]
   static constexpr int kSmemBytes = kOffStats + (2 * kDecWarps + 1) * kDecMaxRows * 4 + 1024;
   static constexpr int kSlabStride = D + 8;                 // floats per merge-slab row (2-way bank conflicts)
-  static_assert(kDecWarps * kDecMaxRows * kSlabStride * 4 <= kStages * kStageBytes,
-                "O merge slabs fit in the ring");
+  static_assert(kDecWarps * kDecMaxRows * kSlabStride * 4 <= kStages * kStageBytes + kWideBytes,
+                "O merge slabs fit in the ring"); 
   static_assert(4 * kStages * 8 + 16 <= 256, "barriers fit");
   static_assert(kMinCtas * (kSmemBytes + 1024) <= 233472, "shared memory per SM");
 };
@@ -125,6 +133,52 @@ struct DecCfg {
 // `rows` rows with the 128-byte swizzle (16-byte chunk index ^ row % 8).
 __device__ __forceinline__ uint32_t swz(int rows, int r, int c) {
   return static_cast<uint32_t>((c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+
+// Four int8 values (a 32-bit word, lowest byte first) widened exactly to two
+// packed pairs of 16-bit floats (lower index in the low half).  fp16: the
+// byte, offset to unsigned, becomes the low mantissa bits of 1024 + u (an
+// fp16 with exponent 10), and 1152 = 1024 + 128 is subtracted; bf16: the same
+// with an fp32 of exponent 23 (2^23 + u, minus 2^23 + 128), then rounded to
+// bf16, which is exact for |x| <= 127.  Both are exact integer arithmetic.
+template <bool BF16>
+__device__ __forceinline__ void widen_s8x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  if constexpr (!BF16) {
+    const __half2 bias = __float2half2_rn(1152.f);
+    uint32_t a = __byte_perm(x, 0x64646464u, 0x4140), b = __byte_perm(x, 0x64646464u, 0x4342);
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias), hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    lo = *reinterpret_cast<uint32_t *>(&ha);
+    hi = *reinterpret_cast<uint32_t *>(&hb);
+  } else {
+    const float f0 = __uint_as_float(__byte_perm(x, 0x4B00u, 0x5440)) - 8388736.f;
+    const float f1 = __uint_as_float(__byte_perm(x, 0x4B00u, 0x5441)) - 8388736.f;
+    const float f2 = __uint_as_float(__byte_perm(x, 0x4B00u, 0x5442)) - 8388736.f;
+    const float f3 = __uint_as_float(__byte_perm(x, 0x4B00u, 0x5443)) - 8388736.f;
+    lo = pack2<true>(f0, f1);
+    hi = pack2<true>(f2, f3);
+  }
+}
+
+// This warp's 16 rows of an int8 tile (64 rows x D bytes, row-major, as the
+// copy left it) widened into the 16-bit staging tile, in the layout of a
+// 64-row box stack with the 128-byte swizzle.
+template <int D, bool BF16>
+__device__ __forceinline__ void widen_rows(uint32_t src, uint32_t dst, int warp, int lane) {
+  constexpr int kChunks = D / 16;  // 16-byte pieces of an int8 row
+#pragma unroll
+  for (int idx = lane; idx < 16 * kChunks; idx += 32) {
+    const int r = warp * 16 + idx / kChunks, c = (idx % kChunks) * 16;
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(src + r * D + c));
+    uint32_t o[8];
+    widen_s8x4<BF16>(w0, o[0], o[1]);
+    widen_s8x4<BF16>(w1, o[2], o[3]);
+    widen_s8x4<BF16>(w2, o[4], o[5]);
+    widen_s8x4<BF16>(w3, o[6], o[7]);
+    st_shared_v4(dst + swz(kDecKeys, r, c), o[0], o[1], o[2], o[3]);
+    st_shared_v4(dst + swz(kDecKeys, r, c + 8), o[4], o[5], o[6], o[7]);
+  }
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -165,10 +219,11 @@ __device__ __forceinline__ void mbar_drain_dec(uint32_t bar, uint32_t parity) {
 
 // Partial attention of one GQA group over one key chunk.  RB = row blocks of
 // 16 (1: up to 16 rows, 2: up to 32); kPaged: K and V come from a page pool.
-template <int D, bool BF16, int RB, bool kPaged>
-__global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
+template <int D, bool BF16, int RB, bool kPaged, bool kQuant = false>
+__global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB, kQuant>::kMinCtas)
     attn_decode_kernel(const __grid_constant__ DecParams p) {
-  using C = DecCfg<D, RB>;
+  static_assert(!(kPaged && kQuant), "int8 K/V is served from a flat cache");
+  using C = DecCfg<D, RB, kQuant>;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,7 +316,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
         break;
       }
       const int s = i % NS, y = k0 + i * kDecKeys;
-      const uint32_t kdst = sKV + s * C::kStageBytes, vdst = kdst + C::kTileBytes;
+      const uint32_t kdst = sKV + s * C::kStageBytes, vdst = kdst + C::kRingTileBytes;
       int slab[kMaxTilePages];
       if constexpr (kPaged) {
         const int page = page_next;
@@ -279,7 +334,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       // one K or V tile into dst: a 64-row box per 64 columns (flat), or per
       // page and 64 columns (paged)
       auto load_tile = [&](uint32_t dst, const CUtensorMap *tm, uint32_t bar) {
-        if constexpr (!kPaged) {
+        if constexpr (kQuant) {
+          tma_load_3d(dst, tm, bar, 0, y, bk);  // int8: one box of 64 rows x D bytes
+        } else if constexpr (!kPaged) {
 #pragma unroll
           for (int cc = 0; cc < D / 64; ++cc) tma_load_3d(dst + cc * C::kBoxBytes, tm, bar, cc * 64, y, bk);
         } else if (pshift >= 6) {
@@ -299,7 +356,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
         break;
       }
       if (elect_one()) {
-        mbar_arrive_expect_tx(bKfull(s), C::kTileBytes);
+        mbar_arrive_expect_tx(bKfull(s), C::kRingTileBytes);
         load_tile(kdst, &p.tmK, bKfull(s));
       }
       __syncwarp();
@@ -309,7 +366,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
         break;
       }
       if (elect_one()) {
-        mbar_arrive_expect_tx(bVfull(s), C::kTileBytes);
+        mbar_arrive_expect_tx(bVfull(s), C::kRingTileBytes);
         load_tile(vdst, &p.tmV, bVfull(s));
       }
       __syncwarp();
@@ -363,7 +420,16 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       ok = false;
       break;
     }
-    const uint32_t sK = sKV + s * C::kStageBytes, sV = sK + C::kTileBytes;
+    uint32_t sK = sKV + s * C::kStageBytes, sV = sK + C::kRingTileBytes;
+    if constexpr (kQuant) {
+      // widen this warp's rows of the int8 K tile, then hand the stage back
+      const uint32_t wide = smem_u32(smem + C::kOffWide);
+      __syncwarp();  // this warp's reads of the previous tile's staging are done
+      widen_rows<D, BF16>(sK, wide, warp, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bKempty(s));
+      sK = wide;
+    }
     const int key_base = k0 + i * kDecKeys + warp * 16;  // this warp's 16 keys
     // ---- S (rows x 16 keys) = Q K^T
     float sc[RB][2][4];
@@ -389,7 +455,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bKempty(s));  // this warp is done with K of tile i
+    if (!kQuant && lane == 0) mbar_arrive(bKempty(s));  // this warp is done with K of tile i
     // ---- mask, online softmax (log2 domain), P as A fragments
     uint32_t pa[RB][4];
 #pragma unroll
@@ -438,6 +504,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       ok = false;
       break;
     }
+    if constexpr (kQuant) {
+      const uint32_t wide = smem_u32(smem + C::kOffWide) + C::kTileBytes;
+      widen_rows<D, BF16>(sV, wide, warp, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bVempty(s));
+      sV = wide;
+    }
     if (kPaged && key_base + 16 > nk) {
       // this warp's V rows past the request's end: zero them (16-byte
       // pieces; a whole 128-byte row of a box is swizzle-free), then order
@@ -465,7 +538,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bVempty(s));  // this warp is done with V of tile i
+    if (!kQuant && lane == 0) mbar_arrive(bVempty(s));  // this warp is done with V of tile i
   }
   // Every thread learns whether any role gave up; then nothing is in flight
   // (the producer drained its copies above).  A CTA that gave up writes no
@@ -539,7 +612,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB>::kMinCtas)
         acc.z += v.z;
         acc.w += v.w;
       }
-      const float inv = rinv[r];
+      const float inv = rinv[r] * p.v_scale;
       const int head = kvh * p.group + r / p.Nq, qi = r % p.Nq;
       const size_t grow = (static_cast<size_t>(b) * p.Hq + head) * p.Nq + qi;
       *reinterpret_cast<float4 *>(p.ws + (grow * p.nchunks + chunk) * D + c) =
