@@ -103,7 +103,7 @@ def normal_tensor(seed: int, shape, dtype: str, scale: float = 1.0) -> torch.Ten
 
 
 def seed_for(config_id: int, layer: int, which: str) -> int:
-    return 1000 * config_id + 10 * layer + {"Q": 0, "K": 1, "V": 2, "L": 3, "P": 4}[which]
+    return 1000 * config_id + 10 * layer + {"Q": 0, "K": 1, "V": 2, "L": 3, "P": 4, "G": 5}[which]
 
 
 @dataclass(frozen=True)
@@ -122,6 +122,7 @@ class AttnShape:
     sm_scale: float | None = None
     key_scale: float = 1.0
     kv_int8: bool = False  # K and V stored as int8 codes with one scale per tensor
+    backward: bool = False  # the call is the backward pass of this forward
 
     @property
     def scale(self) -> float:
@@ -281,6 +282,10 @@ def workload_calls(name: str):
     if name == "mqa_decode_int8":  # mqa_decode's step on an INT8 K/V cache (per-tensor scales)
         return [(AttnShape(4, 32, 1, 1, 8192, 128, "bf16", True, 0, None, kv_int8=True), 8, 0),
                 (AttnShape(4, 32, 8, 1, 8192, 128, "bf16", True, 0, None, kv_int8=True), 8, 1)]
+    if name == "bwd_gpt_layer":  # the backward of a gpt_stack layer (B=8, H=12, N=2048, d=64, bf16, causal)
+        return [(AttnShape(8, 12, 12, 2048, 2048, 64, "bf16", True, 0, 0.125, backward=True), 9, 0)]
+    if name == "bwd_gqa":  # the backward of gqa_mqa's first call (B=4, Hq=32, Hkv=8, N=8192, d=128, bf16, causal)
+        return [(AttnShape(4, 32, 8, 8192, 8192, 128, "bf16", True, 0, None, backward=True), 10, 0)]
     if name == "paged_decode":
         # one decode step on a paged cache of 16-token pages, bf16, d=128, GQA 32/8:
         # the mqa_decode Hkv=8 call with every request at 8192 tokens (same
@@ -292,4 +297,4 @@ def workload_calls(name: str):
 
 
 WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw",
-                  "paged_decode", "mqa_decode_int8"]
+                  "paged_decode", "mqa_decode_int8", "bwd_gpt_layer", "bwd_gqa"]

@@ -50,6 +50,8 @@ WORKLOAD_TEXT = {
     "paged_decode": "decode on a paged cache (16-token pages, shuffled pool), Hq=32, Hkv=8, Nq=1, d=128, bf16: "
                     "B=4 at 8192 tokens; B=32 at drawn lengths 512..8192",
     "mqa_decode_int8": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16 Q, int8 K/V (per-tensor scales)",
+    "bwd_gpt_layer": "backward of a gpt_stack layer: B=8, H=12, N=2048, d=64, bf16, causal, scale 1/8",
+    "bwd_gqa": "backward of B=4, Hq=32, Hkv=8, N=8192, d=128, bf16, causal",
 }
 # Device sources of each kernel family: a committed DRAM-traffic figure
 # (profiles/traffic.json) counts only while they hash to the value recorded
@@ -59,7 +61,14 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd_sm103.cuh", "sm103_ptx.cuh", "fastdiv.h"],
     "attn_decode_kernel": ["attn_decode.cuh", "sm103_ptx.cuh"],
     "attn_short_kernel": ["attn_short.cuh", "sm103_ptx.cuh"],
+    "attn_bwd_kernel": ["attn_bwd_sm103.cuh", "sm103_ptx.cuh"],
 }
+
+
+def metric_name(workload: str) -> str:
+    if workload.startswith("bwd_"):
+        return "attention bwd TFLOP/s (2.5x the forward's FLOPs)"
+    return "attention fwd TFLOP/s"
 
 
 def parse_args():
@@ -201,8 +210,8 @@ def call_label(s) -> str:
     if isinstance(s, ai.PagedShape):
         return (f"paged_B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_L{s.max_seq_len}_ps{s.page_size}_d{s.d}_{s.dtype}"
                 f"_c{int(s.causal)}_w{s.window}")
-    return (f"B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}{'_kv8' if s.kv_int8 else ''}"
-            f"_c{int(s.causal)}_w{s.window}")
+    return (f"{'bwd_' if s.backward else ''}B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}"
+            f"{'_kv8' if s.kv_int8 else ''}_c{int(s.causal)}_w{s.window}")
 
 
 def prepare_paged(shape, cid, layer, device):
@@ -229,6 +238,32 @@ def prepare_paged(shape, cid, layer, device):
     return c
 
 
+def prepare_bwd(shape, cid, layer, device):
+    """One backward call: seeded Q, K, V and upstream gradient; O and LSE
+    from the library's forward (computed here, before any timing)."""
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+    do = ai.normal_tensor(ai.seed_for(cid, layer, "G"), tuple(q.shape), shape.dtype)
+    c = {"shape": shape, "backward": True, "q_host": q, "k_host": k, "v_host": v, "do_host": do,
+         "q": q.to(device), "k": k.to(device), "v": v.to(device), "do": do.to(device)}
+    c["o"], c["lse"] = attn.flash_attn_forward(c["q"], c["k"], c["v"], causal=shape.causal, window=shape.window,
+                                               sm_scale=shape.scale)
+    torch.cuda.synchronize(device)
+    c["o_host"], c["lse_host"] = c["o"].cpu(), c["lse"].cpu()
+    c["dq"], c["dk"], c["dv"] = torch.empty_like(c["q"]), torch.empty_like(c["k"]), torch.empty_like(c["v"])
+    c["dtype_code"] = attn.ATTN_DTYPE_BF16 if shape.dtype == "bf16" else attn.ATTN_DTYPE_FP16
+    c["flops"] = acc.shape_flops(shape)
+    c["bytes"] = acc.shape_bytes(shape)
+    c["label"] = call_label(shape)
+    c["ws"] = torch.empty(attn.attn_bwd_workspace_bytes(shape.B, shape.Hq, shape.Nq, shape.d), dtype=torch.uint8,
+                          device=device)
+    c["path"] = None
+    c["kernel"] = "attn_bwd_kernel"
+    c["launches"] = 3  # D and the accumulator, the gradients, dQ
+    return c
+
+
 def prepare(workload: str, device):
     import tiled_attention_forward_fwd_gb300 as attn
 
@@ -236,6 +271,9 @@ def prepare(workload: str, device):
     for shape, cid, layer in ai.workload_calls(workload):
         if isinstance(shape, ai.PagedShape):
             calls.append(prepare_paged(shape, cid, layer, device))
+            continue
+        if shape.backward:
+            calls.append(prepare_bwd(shape, cid, layer, device))
             continue
         if shape.kv_int8:
             q, k, ks, v, vs = ai.make_qkv_int8(shape, cid, layer)
@@ -273,6 +311,14 @@ def launch(c, stream_handle):
 
     s = c["shape"]
     ws = c["ws"]
+    if c.get("backward"):
+        st = attn.attn_bwd(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["o"].data_ptr(),
+                           c["do"].data_ptr(), c["lse"].data_ptr(), c["dq"].data_ptr(), c["dk"].data_ptr(),
+                           c["dv"].data_ptr(), s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale,
+                           c["dtype_code"], ws.data_ptr(), ws.numel(), stream_handle)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_bwd failed: {attn.attn_status_string(st)}")
+        return
     if c.get("paged"):
         st = attn.attn_fwd_paged(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["table"].data_ptr(),
                                  c["lens"].data_ptr(), c["o"].data_ptr(), c["lse"].data_ptr(), s.B, s.Hq, s.Hkv,
@@ -390,6 +436,13 @@ def e2e_timing(calls, steps, warmup, device, stream):
     need = 0
     for c in calls:
         s = c["shape"]
+        if c.get("backward"):
+            # Q, K, V, O, dO and LSE copied in; dQ, dK, dV copied back
+            ph = {k: c[k + "_host"].pin_memory() for k in ("q", "k", "v", "o", "do", "lse")}
+            for k in ("dq", "dk", "dv"):
+                ph[k] = torch.empty(c[k].shape, dtype=c[k].dtype).pin_memory()
+            pinned.append(ph)
+            continue
         if c.get("paged") or s.kv_int8:
             # the inputs of a paged call (pools, table, lengths, Q) or of an
             # int8 call (Q, codes) are copied into its device tensors, then
@@ -410,6 +463,10 @@ def e2e_timing(calls, steps, warmup, device, stream):
     h2d = d2h = 0
     for c in calls:
         s = c["shape"]
+        if c.get("backward"):
+            h2d += (2 * c["q"].numel() + c["k"].numel() + c["v"].numel() + c["do"].numel()) * 2 + c["lse"].numel() * 4
+            d2h += (c["dq"].numel() + c["dk"].numel() + c["dv"].numel()) * 2
+            continue
         h2d += c["q"].numel() * 2 + (c["k"].numel() + c["v"].numel()) * c["k"].element_size()
         if c.get("paged"):
             h2d += (c["table"].numel() + c["lens"].numel()) * 4
@@ -418,6 +475,14 @@ def e2e_timing(calls, steps, warmup, device, stream):
     def one_step():
         for c, ph in zip(calls, pinned):
             s = c["shape"]
+            if c.get("backward"):
+                with torch.cuda.stream(stream):
+                    for k in ("q", "k", "v", "o", "do", "lse"):
+                        c[k].copy_(ph[k], non_blocking=True)
+                    launch(c, stream.cuda_stream)
+                    for k in ("dq", "dk", "dv"):
+                        ph[k].copy_(c[k], non_blocking=True)
+                continue
             if c.get("paged") or s.kv_int8:
                 with torch.cuda.stream(stream):
                     for k in (("q", "k", "v", "table", "lens") if c.get("paged") else ("q", "k", "v")):
@@ -442,10 +507,11 @@ def e2e_timing(calls, steps, warmup, device, stream):
     t1.record(stream)
     stream.synchronize()
     ms = t0.elapsed_time(t1) / steps
-    # result check on the last step: the copied-back O equals the device path's O
+    # result check on the last step: what was copied back equals the device tensors
     for c, ph in zip(calls, pinned):
-        if not torch.equal(ph["o"], c["o"].cpu()):
-            raise RuntimeError("host-buffer path disagrees with the device path")
+        for k in (("dq", "dk", "dv") if c.get("backward") else ("o",)):
+            if not torch.equal(ph[k], c[k].cpu()):
+                raise RuntimeError("host-buffer path disagrees with the device path")
     return ms, h2d, d2h
 
 
@@ -466,6 +532,11 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
             q, k, v, table, lens = ai.make_paged(shape, cid, layer)
             prepared.append((shape, q, k.to(torch.float64), v.to(torch.float64), table, lens))
             continue
+        if shape.backward:
+            q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+            do = ai.normal_tensor(ai.seed_for(cid, layer, "G"), tuple(q.shape), shape.dtype)
+            prepared.append((shape, q, k, v, do, "bwd"))
+            continue
         if shape.kv_int8:  # the oracle reads the exactly dequantised cache
             q, kc, ks, vc, vs = ai.make_qkv_int8(shape, cid, layer)
             k, v = kc.to(torch.float64) * ks, vc.to(torch.float64) * vs
@@ -485,11 +556,30 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
 
     covered = []  # per call of the last run: the whole call was sampled
 
+    def run_bwd(shape, q, k, v, do, rows_per_call):
+        # the oracle's gradients of a self-contained piece of the call: batch
+        # 0, the first GQA group, the first n positions (a causal prefix
+        # sees only itself; non-causal: its own keys)
+        g = shape.Hq // shape.Hkv
+        n = max(1, min(shape.Nq, rows_per_call // g))
+        covered.append(n == shape.Nq and shape.B == 1 and shape.Hkv == 1)
+        sub = ai.AttnShape(1, g, 1, n, n, shape.d, shape.dtype, shape.causal, shape.window, shape.sm_scale,
+                           backward=True)
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q[:1, :g, :n], k[:1, :1, :n], v[:1, :1, :n], do[:1, :g, :n], causal=shape.causal,
+                             window=shape.window, sm_scale=shape.scale)
+        return acc.shape_flops(sub, exact=True), time.perf_counter() - t0
+
     def run(rows_per_call):
         flops = 0.0
         t = 0.0
         covered.clear()
         for shape, *tensors in prepared:
+            if tensors and isinstance(tensors[-1], str):
+                f, dt = run_bwd(shape, *tensors[:-1], rows_per_call)
+                flops += f
+                t += dt
+                continue
             if isinstance(shape, ai.PagedShape):
                 f, dt = run_paged(shape, *tensors, rows_per_call)
                 flops += f
@@ -550,7 +640,7 @@ def reference_arm(args):
         secs += t
     value = flops / secs / 1e12
     line = {
-        "impl": "reference", "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -641,7 +731,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": steps,
+            "metric": metric_name(args.workload), "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": steps,
             "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": calls[0]["shape"].dtype, "data": "synthetic",
             "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",

@@ -250,6 +250,33 @@ attn_status_t attn_fwd_kv_int8(const void *Q, const void *K_codes, const void *V
                                int causal, int window, float sm_scale, attn_dtype_t dtype, void *workspace,
                                size_t workspace_bytes, cudaStream_t stream);
 
+/* Backward pass: the gradients of the forward definition for an upstream
+ * gradient dO (the pages store the log-sum-exp "for the backward pass":
+ * cruxr.ai "FlashAttention: Nunca materializar la matriz de atencion", lab 02
+ * kernel skeleton; the pages defer the backward itself).  With P recomputed
+ * tile by tile from Q, K and the forward's LSE, P = exp(sm_scale * Q K^T -
+ * LSE) (masked entries 0):
+ *   dV = P^T dO,   dS = P o (dO V^T - D) with D = rowsum(dO o O),
+ *   dK = sm_scale * dS^T Q,   dQ = sm_scale * dS K,
+ * dK and dV summed over the query heads of each K/V head.  P and dS are
+ * rounded to the input dtype before their products, as the forward rounds P.
+ *
+ * Q, K, V, causal, window, sm_scale, dtype: those of the forward call.  O
+ *   (B x Hq x Nq x d) and LSE (fp32, B x Hq x Nq, required): its outputs.
+ *   dO (B x Hq x Nq x d): the upstream gradient.  dQ (like Q), dK, dV (like
+ *   K): outputs, fully written.  All DEVICE, 16-byte aligned.
+ * workspace (DEVICE, 16-byte aligned, required): at least
+ *   attn_bwd_workspace_bytes(B, Hq, Nq, d) bytes (an fp32 dQ accumulator and
+ *   D), not used by an overlapping call; its contents need no
+ *   initialisation.  Three kernels are enqueued on `stream` (D and the
+ *   accumulator; the gradients; dQ); nothing is allocated; no sync.
+ * Errors as attn_fwd_ex; B * Hkv must not exceed 65535. */
+attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                       void *dQ, void *dK, void *dV, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                       int window, float sm_scale, attn_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq, int d);
+
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.

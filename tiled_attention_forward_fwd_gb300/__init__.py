@@ -36,7 +36,7 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
-            "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8"]
+            "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8", "attn_bwd", "attn_bwd_workspace_bytes"]
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.attn_set_test_stall.restype = None
         L.attn_fwd_kv_int8.argtypes = [vp, vp, vp, cf, cf, vp, vp] + [ci] * 8 + [cf, ci, vp, sz, vp]
         L.attn_fwd_kv_int8.restype = ci
+        L.attn_bwd.argtypes = [vp] * 9 + [ci] * 8 + [cf, ci, vp, sz, vp]
+        L.attn_bwd.restype = ci
+        L.attn_bwd_workspace_bytes.argtypes = [ci] * 4
+        L.attn_bwd_workspace_bytes.restype = sz
         L.attn_status_string.argtypes = [ci]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_abi_version.argtypes = []
@@ -161,6 +165,16 @@ def attn_fwd_kv_int8(Q, K_codes, V_codes, k_scale, v_scale, O, LSE, B, Hq, Hkv, 
     return lib().attn_fwd_kv_int8(Q, K_codes, V_codes, float(k_scale), float(v_scale), O, LSE, B, Hq, Hkv, Nq, Nk, d,
                                   int(causal), int(window), float(sm_scale), int(dtype), workspace,
                                   int(workspace_bytes), stream)
+
+
+def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, workspace,
+             workspace_bytes, stream) -> int:
+    return lib().attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Nq, Nk, d, int(causal), int(window),
+                          float(sm_scale), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_bwd_workspace_bytes(B, Hq, Nq, d) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, Hq, Nq, d))
 
 
 def attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d) -> int:
@@ -348,10 +362,39 @@ def flash_attn_kv_int8(q, k_codes, v_codes, k_scale: float, v_scale: float, caus
     return out, (lse if return_lse else None)
 
 
+def flash_attn_backward(q, k, v, o, lse, do, causal: bool = False, window: int = 0, sm_scale: float | None = None,
+                        workspace=None):
+    """Gradients (dQ, dK, dV) of O = softmax(sm_scale * q k^T + mask) v for an
+    upstream gradient ``do`` (see attn_bwd in include/attn.h).  ``o`` and
+    ``lse`` are the forward's outputs for the same arguments.  dK and dV sum
+    the query heads of each K/V head.  Runs on the current stream."""
+    torch = _torch()
+    ts = (q, k, v, o, do)
+    if not all(t.is_cuda for t in ts) or not lse.is_cuda:
+        raise ValueError("flash_attn_backward needs CUDA tensors (no CPU path)")
+    if not all(t.dtype == q.dtype for t in ts) or lse.dtype != torch.float32:
+        raise TypeError("q, k, v, o, do must share a dtype; lse must be float32")
+    q, k, v, o, do, lse = (t.contiguous() for t in (q, k, v, o, do, lse))
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if o.shape != q.shape or do.shape != q.shape or v.shape != k.shape or lse.shape != (B, Hq, Nq):
+        raise ValueError("inconsistent shapes")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(max(attn_bwd_workspace_bytes(B, Hq, Nq, d), 16), dtype=torch.uint8, device=q.device)
+    st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Nq, Nk, d, causal, window, scale,
+                  _dtype_code(q), workspace.data_ptr(), workspace.numel(), _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and read/clear the kernel status word."""
     return attn_device_status(_stream_handle(device))
 
 
-__all__ = EXPORTED + ["flash_attn_forward", "flash_attn_paged", "flash_attn_kv_int8", "device_status", "lib",
-                      "AttnError"]
+__all__ = EXPORTED + ["flash_attn_forward", "flash_attn_paged", "flash_attn_kv_int8", "flash_attn_backward",
+                      "device_status", "lib", "AttnError"]

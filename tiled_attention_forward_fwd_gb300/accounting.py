@@ -58,11 +58,19 @@ def compulsory_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, elem_b
 
 
 def shape_flops(s, exact: bool = False) -> float:
+    """The forward's FLOPs; for a backward call (s.backward) 2.5 times as
+    many: five matrix products of the forward's size (S, dP, dV, dK, dQ)
+    against its two."""
     f = exact_flops if exact else metric_flops
-    return f(s.B, s.Hq, s.Nq, s.Nk, s.d, s.causal, s.window)
+    fw = f(s.B, s.Hq, s.Nq, s.Nk, s.d, s.causal, s.window)
+    return 2.5 * fw if getattr(s, "backward", False) else fw
 
 
 def shape_bytes(s, with_lse: bool = True) -> int:
+    if getattr(s, "backward", False):
+        # reads Q, O, dO and K, V; writes dQ and dK, dV; reads the LSE
+        b = 2 * s.d * (4 * s.B * s.Hq * s.Nq + 4 * s.B * s.Hkv * s.Nk)
+        return b + (4 * s.B * s.Hq * s.Nq if with_lse else 0)
     if getattr(s, "kv_int8", False):  # Q and O 16-bit, K and V one byte per element
         b = 2 * s.d * 2 * s.B * s.Hq * s.Nq + s.d * 2 * s.B * s.Hkv * s.Nk
         return b + (4 * s.B * s.Hq * s.Nq if with_lse else 0)

@@ -17,6 +17,7 @@
 #include "../../include/attn.h"
 #include "attn_decode.cuh"
 #include "attn_short.cuh"
+#include "attn_bwd_sm103.cuh"
 #include "attn_fwd_sm103.cuh"
 
 namespace attn {
@@ -356,6 +357,68 @@ static attn_status_t dispatch_prefill(const void *Q, const void *K, const void *
                              : launch_prefill<64, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg);
   return bf16 ? launch_prefill<128, true>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg)
               : launch_prefill<128, false>(Q, K, V, O, LSE, s, ws, ws_bytes, stream, pg);
+}
+
+// ---------------------------------------------------------------- backward
+static size_t bwd_ws_bytes(long long rows, int d) {
+  return round_up256(static_cast<size_t>(rows) * d * 4) + round_up256(static_cast<size_t>(rows) * 4);
+}
+
+template <int D, bool BF16>
+static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                const float *LSE, void *dQ, void *dK, void *dV, const Shape &s, void *ws,
+                                cudaStream_t stream) {
+  using Cfg = BwdCfg<D>;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long zq = static_cast<long long>(s.B) * s.Hq, zk = static_cast<long long>(s.B) * s.Hkv;
+  if (!make_map(&p.tmQ, Q, D, s.Nq, zq, BF16) || !make_map(&p.tmDO, dO, D, s.Nq, zq, BF16) ||
+      !make_map(&p.tmK, K, D, s.Nk, zk, BF16) || !make_map(&p.tmV, V, D, s.Nk, zk, BF16))
+    return ATTN_ERR_CUDA;
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  const long long rows = zq * s.Nq;
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  p.dq_acc = reinterpret_cast<float *>(base);
+  p.delta = reinterpret_cast<const float *>(base + round_up256(static_cast<size_t>(rows) * D * 4));
+  p.lse = LSE;
+  p.dK = dK;
+  p.dV = dV;
+  p.status = status;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Nq = s.Nq;
+  p.Nk = s.Nk;
+  p.group = s.Hq / s.Hkv;
+  p.causal = s.causal ? 1 : 0;
+  p.window = s.window;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  p.sm_scale = s.sm_scale;
+  p.timeout_ns = g_timeout_ns.load();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  static std::once_flag once[64];
+  static bool ready[64];
+  std::call_once(once[dev], [&] {
+    ready[dev] = cudaFuncSetAttribute(attn_bwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg::kSmemBytes) == cudaSuccess;
+  });
+  if (!ready[dev]) return ATTN_ERR_UNSUPPORTED;
+  float *delta = reinterpret_cast<float *>(base + round_up256(static_cast<size_t>(rows) * D * 4));
+  if (launch_pdl(attn_bwd_prep_kernel<D, BF16>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, stream, O,
+                 dO, delta, p.dq_acc, rows) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>((s.Nk + 127) / 128), static_cast<unsigned>(zk));
+  if (launch_pdl(attn_bwd_kernel<D, BF16>, grid, dim3(kBwdThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const long long n4 = rows * D / 4;
+  const int sms = std::max(1, device_sm_count());
+  const long long blocks = std::min<long long>((n4 + 255) / 256, 8LL * sms);
+  if (launch_pdl(attn_bwd_dq_kernel<BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                 static_cast<const float *>(p.dq_acc), dQ, n4, s.sm_scale) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- split-KV (decode) path
@@ -756,6 +819,32 @@ attn_status_t attn_fwd_kv_int8(const void *Q, const void *K_codes, const void *V
   if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   const QuantKV qk{k_scale, v_scale};
   return dispatch_decode(Q, K_codes, V_codes, O, LSE, s, pl, static_cast<float *>(workspace), stream, nullptr, &qk);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq, int d) {
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || (d != 64 && d != 128)) return 0;
+  return bwd_ws_bytes(static_cast<long long>(B) * Hq * Nq, d);
+}
+
+attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                       void *dQ, void *dK, void *dV, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                       int window, float sm_scale, attn_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  Shape s{B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype};
+  attn_status_t st = validate(Q, K, V, O, LSE, s);
+  if (st != ATTN_OK) return st;
+  if (!dO || !dQ || !dK || !dV || !LSE || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+    return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Hkv > 65535) return ATTN_ERR_INVALID_ARG;  // grid.y
+  const size_t need = bwd_ws_bytes(static_cast<long long>(B) * Hq * Nq, d);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  const bool bf16 = dtype == ATTN_DTYPE_BF16;
+  if (d == 64)
+    return bf16 ? launch_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream)
+                : launch_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream);
+  return bf16 ? launch_bwd<128, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream)
+              : launch_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream);
 }
 
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
