@@ -123,6 +123,7 @@ class AttnShape:
     key_scale: float = 1.0
     kv_int8: bool = False  # K and V stored as int8 codes with one scale per tensor
     backward: bool = False  # the call is the backward pass of this forward
+    mla: bool = False  # latent attention: Hkv = 1, d = d_c, K = V = the latent cache, Q the absorbed queries
 
     @property
     def scale(self) -> float:
@@ -286,6 +287,13 @@ def workload_calls(name: str):
         return [(AttnShape(8, 12, 12, 2048, 2048, 64, "bf16", True, 0, 0.125, backward=True), 9, 0)]
     if name == "bwd_gqa":  # the backward of gqa_mqa's first call (B=4, Hq=32, Hkv=8, N=8192, d=128, bf16, causal)
         return [(AttnShape(4, 32, 8, 8192, 8192, 128, "bf16", True, 0, None, backward=True), 10, 0)]
+    if name == "mla_decode":
+        # one decode step of latent attention at the latent-attention section's
+        # DeepSeek-V2 sizes (n_h = 128 heads, d_c = 512, scale 1/sqrt(d_h),
+        # d_h = 128) on the motivation page's batch of 32 requests x 8192
+        # tokens; then the same step with 4 queries per head (speculative decode)
+        return [(AttnShape(32, 128, 1, 1, 8192, 512, "bf16", True, 0, 1.0 / math.sqrt(128), mla=True), 11, 0),
+                (AttnShape(8, 128, 1, 4, 8192, 512, "bf16", True, 0, 1.0 / math.sqrt(128), mla=True), 11, 1)]
     if name == "paged_decode":
         # one decode step on a paged cache of 16-token pages, bf16, d=128, GQA 32/8:
         # the mqa_decode Hkv=8 call with every request at 8192 tokens (same
@@ -297,4 +305,4 @@ def workload_calls(name: str):
 
 
 WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw",
-                  "paged_decode", "mqa_decode_int8", "bwd_gpt_layer", "bwd_gqa"]
+                  "paged_decode", "mqa_decode_int8", "bwd_gpt_layer", "bwd_gqa", "mla_decode"]

@@ -52,6 +52,8 @@ WORKLOAD_TEXT = {
     "mqa_decode_int8": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16 Q, int8 K/V (per-tensor scales)",
     "bwd_gpt_layer": "backward of a gpt_stack layer: B=8, H=12, N=2048, d=64, bf16, causal, scale 1/8",
     "bwd_gqa": "backward of B=4, Hq=32, Hkv=8, N=8192, d=128, bf16, causal",
+    "mla_decode": "latent attention with absorbed queries, d_c=512, n_h=128, bf16, causal, scale 1/sqrt(128): "
+                  "B=32, Nq=1, Nk=8192; B=8, Nq=4, Nk=8192",
 }
 # Device sources of each kernel family: a committed DRAM-traffic figure
 # (profiles/traffic.json) counts only while they hash to the value recorded
@@ -62,6 +64,7 @@ KERNEL_SOURCES = {
     "attn_decode_kernel": ["attn_decode.cuh", "sm103_ptx.cuh"],
     "attn_short_kernel": ["attn_short.cuh", "sm103_ptx.cuh"],
     "attn_bwd_kernel": ["attn_bwd_sm103.cuh", "sm103_ptx.cuh"],
+    "attn_mla_kernel": ["attn_mla.cuh", "attn_decode.cuh", "sm103_ptx.cuh"],
 }
 
 
@@ -211,7 +214,7 @@ def call_label(s) -> str:
         return (f"paged_B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_L{s.max_seq_len}_ps{s.page_size}_d{s.d}_{s.dtype}"
                 f"_c{int(s.causal)}_w{s.window}")
     return (f"{'bwd_' if s.backward else ''}B{s.B}_Hq{s.Hq}_Hkv{s.Hkv}_Nq{s.Nq}_Nk{s.Nk}_d{s.d}_{s.dtype}"
-            f"{'_kv8' if s.kv_int8 else ''}_c{int(s.causal)}_w{s.window}")
+            f"{'_kv8' if s.kv_int8 else ''}{'_mla' if s.mla else ''}_c{int(s.causal)}_w{s.window}")
 
 
 def prepare_paged(shape, cid, layer, device):
@@ -264,6 +267,28 @@ def prepare_bwd(shape, cid, layer, device):
     return c
 
 
+def prepare_mla(shape, cid, layer, device):
+    """One latent-attention call: absorbed queries (B, n_h, Nq, 512) and the
+    latent cache (B, Nk, 512), drawn as Q and the single K/V head."""
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    q, k, _ = ai.make_qkv(shape, config_id=cid, layer=layer)
+    c = {"shape": shape, "mla": True, "q_host": q, "c_host": k[:, 0].contiguous(), "q": q.to(device)}
+    c["c"] = c["c_host"].to(device)
+    c["o"] = torch.empty_like(c["q"])
+    c["lse"] = torch.empty((shape.B, shape.Hq, shape.Nq), device=device, dtype=torch.float32)
+    c["dtype_code"] = attn.ATTN_DTYPE_BF16 if shape.dtype == "bf16" else attn.ATTN_DTYPE_FP16
+    c["flops"] = acc.shape_flops(shape)
+    c["bytes"] = acc.shape_bytes(shape)
+    c["label"] = call_label(shape)
+    c["ws"] = torch.empty(attn.attn_fwd_mla_workspace_bytes(shape.B, shape.Hq, shape.Nq, shape.Nk, shape.d),
+                          dtype=torch.uint8, device=device)
+    c["path"] = None
+    c["kernel"] = "attn_mla_kernel"
+    c["launches"] = 2  # the split kernel, the merge
+    return c
+
+
 def prepare(workload: str, device):
     import tiled_attention_forward_fwd_gb300 as attn
 
@@ -274,6 +299,9 @@ def prepare(workload: str, device):
             continue
         if shape.backward:
             calls.append(prepare_bwd(shape, cid, layer, device))
+            continue
+        if shape.mla:
+            calls.append(prepare_mla(shape, cid, layer, device))
             continue
         if shape.kv_int8:
             q, k, ks, v, vs = ai.make_qkv_int8(shape, cid, layer)
@@ -327,6 +355,13 @@ def launch(c, stream_handle):
                                  stream_handle)
         if st != attn.ATTN_OK:
             raise RuntimeError(f"attn_fwd_paged failed: {attn.attn_status_string(st)}")
+        return
+    if c.get("mla"):
+        st = attn.attn_fwd_mla(c["q"].data_ptr(), c["c"].data_ptr(), c["o"].data_ptr(), c["lse"].data_ptr(), s.B,
+                               s.Hq, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale, c["dtype_code"], ws.data_ptr(),
+                               ws.numel(), stream_handle)
+        if st != attn.ATTN_OK:
+            raise RuntimeError(f"attn_fwd_mla failed: {attn.attn_status_string(st)}")
         return
     if s.kv_int8:
         st = attn.attn_fwd_kv_int8(c["q"].data_ptr(), c["k"].data_ptr(), c["v"].data_ptr(), c["k_scale"],
@@ -443,11 +478,15 @@ def e2e_timing(calls, steps, warmup, device, stream):
                 ph[k] = torch.empty(c[k].shape, dtype=c[k].dtype).pin_memory()
             pinned.append(ph)
             continue
-        if c.get("paged") or s.kv_int8:
-            # the inputs of a paged call (pools, table, lengths, Q) or of an
-            # int8 call (Q, codes) are copied into its device tensors, then
-            # the call runs on them
-            names = ("q", "k", "v", "table", "lens") if c.get("paged") else ("q", "k", "v")
+        if c.get("paged") or c.get("mla") or s.kv_int8:
+            # the inputs of a paged call (pools, table, lengths, Q), of a
+            # latent call (Q, latent cache) or of an int8 call (Q, codes) are
+            # copied into its device tensors, then the call runs on them
+            names = ("q", "k", "v")
+            if c.get("paged"):
+                names = ("q", "k", "v", "table", "lens")
+            elif c.get("mla"):
+                names = ("q", "c")
             ph = {k: c[k + "_host"].pin_memory() for k in names}
             ph["o"] = torch.empty_like(ph["q"]).pin_memory()
             ph["lse"] = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32).pin_memory()
@@ -467,6 +506,10 @@ def e2e_timing(calls, steps, warmup, device, stream):
             h2d += (2 * c["q"].numel() + c["k"].numel() + c["v"].numel() + c["do"].numel()) * 2 + c["lse"].numel() * 4
             d2h += (c["dq"].numel() + c["dk"].numel() + c["dv"].numel()) * 2
             continue
+        if c.get("mla"):
+            h2d += (c["q"].numel() + c["c"].numel()) * 2
+            d2h += c["o"].numel() * 2 + s.B * s.Hq * s.Nq * 4
+            continue
         h2d += c["q"].numel() * 2 + (c["k"].numel() + c["v"].numel()) * c["k"].element_size()
         if c.get("paged"):
             h2d += (c["table"].numel() + c["lens"].numel()) * 4
@@ -483,9 +526,11 @@ def e2e_timing(calls, steps, warmup, device, stream):
                     for k in ("dq", "dk", "dv"):
                         ph[k].copy_(c[k], non_blocking=True)
                 continue
-            if c.get("paged") or s.kv_int8:
+            if c.get("paged") or c.get("mla") or s.kv_int8:
+                names = ("q", "k", "v", "table", "lens") if c.get("paged") else ("q", "c") if c.get("mla") \
+                    else ("q", "k", "v")
                 with torch.cuda.stream(stream):
-                    for k in (("q", "k", "v", "table", "lens") if c.get("paged") else ("q", "k", "v")):
+                    for k in names:
                         c[k].copy_(ph[k], non_blocking=True)
                     launch(c, stream.cuda_stream)
                     ph["o"].copy_(c["o"], non_blocking=True)
@@ -542,6 +587,8 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
             k, v = kc.to(torch.float64) * ks, vc.to(torch.float64) * vs
         else:
             q, k, v = ai.make_qkv(shape, config_id=cid, layer=layer)
+            if shape.mla:  # the latent cache serves as keys and values
+                v = k
         prepared.append((shape, q.reshape(-1, shape.d), k.to(torch.float64), v.to(torch.float64)))
 
     def run_paged(shape, q, k, v, table, lens, rows_per_call):

@@ -277,6 +277,39 @@ attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *
                        cudaStream_t stream);
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq, int d);
 
+/* Attention over a latent K/V cache with absorbed queries (Multi-Head
+ * Latent Attention; cruxr.ai "Optimizaciones de Atencion", section
+ * "Multi-Head Latent Attention (MLA)").  Each token caches one latent vector
+ * c_t of d_c values; head h's keys and values are c W_K,h and c W_V,h.  With
+ * the up-projections absorbed (the same section: the attention is rewritten
+ * to work on the compressed form), head h's score for token t is
+ * sm_scale * (q~_h . c_t) with q~_h = W_K,h q_h, and its output is o~_h W_V,h
+ * with o~_h = sum_t P_t c_t.  This call computes o~ and the log-sum-exp for
+ * every head and query: standard attention with one K/V head whose keys and
+ * values are both the latent vectors.  The projections themselves (q -> q~,
+ * o~ -> o) are ordinary matrix products outside this call.
+ *
+ * Q_lat (DEVICE, B x n_h x Nq x d_c, dense, dtype): the absorbed queries q~.
+ * C_lat (DEVICE, B x Nk x d_c, dense, dtype): the latent cache.
+ * O_lat (DEVICE, B x n_h x Nq x d_c, dense, written): o~.
+ * LSE (DEVICE fp32 B x n_h x Nq, natural log; may be NULL).
+ * d_c: 512 (the width of the page's example); other values return
+ *   ATTN_ERR_UNSUPPORTED.  causal / window / sm_scale as attn_fwd_ex, with
+ *   query i of every head at position Nk - Nq + i (the last Nq tokens).
+ * workspace (DEVICE, required, 16-byte aligned): at least
+ *   attn_fwd_mla_workspace_bytes(...) bytes; the partial results of the key
+ *   chunks, fully overwritten by every call (no initialisation needed).
+ * Pointers 16-byte aligned, else ATTN_ERR_INVALID_ARG.  Two launches on
+ * `stream` (the split kernel, then the merge); nothing is allocated; the call
+ * does not synchronise. */
+attn_status_t attn_fwd_mla(const void *Q_lat, const void *C_lat, void *O_lat, float *LSE, int B, int n_h, int Nq,
+                           int Nk, int d_c, int causal, int window, float sm_scale, attn_dtype_t dtype,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes attn_fwd_mla wants for these sizes on the current device;
+ * 0 when the sizes are invalid or d_c is not 512.  No device work. */
+size_t attn_fwd_mla_workspace_bytes(int B, int n_h, int Nq, int Nk, int d_c);
+
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into
  * the caller's DEVICE staging buffer `dev_buf`, runs attn_fwd_ex, and copies O
  * (and LSE when non-NULL) back into HOST memory, all enqueued on `stream`.

@@ -36,7 +36,8 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_device_status", "attn_set_wait_timeout_ns", "attn_status_string", "attn_abi_version",
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
-            "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8", "attn_bwd", "attn_bwd_workspace_bytes"]
+            "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8", "attn_bwd", "attn_bwd_workspace_bytes",
+            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes"]
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +81,10 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.restype = ci
         L.attn_bwd_workspace_bytes.argtypes = [ci] * 4
         L.attn_bwd_workspace_bytes.restype = sz
+        L.attn_fwd_mla.argtypes = [vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp, sz, vp]
+        L.attn_fwd_mla.restype = ci
+        L.attn_fwd_mla_workspace_bytes.argtypes = [ci] * 5
+        L.attn_fwd_mla_workspace_bytes.restype = sz
         L.attn_status_string.argtypes = [ci]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_abi_version.argtypes = []
@@ -175,6 +180,16 @@ def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Nq, Nk, d, causal, win
 
 def attn_bwd_workspace_bytes(B, Hq, Nq, d) -> int:
     return int(lib().attn_bwd_workspace_bytes(B, Hq, Nq, d))
+
+
+def attn_fwd_mla(Q_lat, C_lat, O_lat, LSE, B, n_h, Nq, Nk, d_c, causal, window, sm_scale, dtype, workspace,
+                 workspace_bytes, stream) -> int:
+    return lib().attn_fwd_mla(Q_lat, C_lat, O_lat, LSE, B, n_h, Nq, Nk, d_c, int(causal), int(window),
+                              float(sm_scale), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_fwd_mla_workspace_bytes(B, n_h, Nq, Nk, d_c) -> int:
+    return int(lib().attn_fwd_mla_workspace_bytes(B, n_h, Nq, Nk, d_c))
 
 
 def attn_fwd_paged_workspace_bytes(B, Hq, Hkv, Nq, max_seq_len, d) -> int:
@@ -359,6 +374,42 @@ def flash_attn_kv_int8(q, k_codes, v_codes, k_scale: float, v_scale: float, caus
                           _dtype_code(q), workspace.data_ptr(), workspace.numel(), _stream_handle(q.device))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_kv_int8")
+    return out, (lse if return_lse else None)
+
+
+def flash_attn_mla(q_lat, c_lat, causal: bool = True, window: int = 0, sm_scale: float | None = None,
+                   return_lse: bool = True, out=None, lse=None, workspace=None):
+    """Attention over a latent cache with absorbed queries (see attn_fwd_mla
+    in include/attn.h).  q_lat: (B, n_h, Nq, d_c) fp16 or bf16, the absorbed
+    queries; c_lat: (B, Nk, d_c), same dtype and device; d_c = 512.
+    ``sm_scale`` defaults to 1/sqrt(d_c); a model passes its own (the head
+    dimension's).  Returns ``(O_lat, LSE)``, O_lat (B, n_h, Nq, d_c).  Runs on
+    the current stream."""
+    torch = _torch()
+    if not (q_lat.is_cuda and c_lat.is_cuda):
+        raise ValueError("flash_attn_mla needs CUDA tensors (no CPU path)")
+    if q_lat.dtype != c_lat.dtype:
+        raise TypeError("q_lat and c_lat must share a dtype")
+    if q_lat.dim() != 4 or c_lat.dim() != 3:
+        raise ValueError("q_lat must be (B,n_h,Nq,d_c) and c_lat (B,Nk,d_c)")
+    q_lat, c_lat = q_lat.contiguous(), c_lat.contiguous()
+    B, n_h, Nq, d_c = q_lat.shape
+    Nk = c_lat.shape[1]
+    if c_lat.shape[0] != B or c_lat.shape[2] != d_c:
+        raise ValueError("c_lat batch / latent width do not match q_lat")
+    scale = float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(d_c)
+    if out is None:
+        out = torch.empty_like(q_lat)
+    if return_lse and lse is None:
+        lse = torch.empty((B, n_h, Nq), device=q_lat.device, dtype=torch.float32)
+    if workspace is None:
+        need = attn_fwd_mla_workspace_bytes(B, n_h, Nq, Nk, d_c)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_lat.device)
+    st = attn_fwd_mla(q_lat.data_ptr(), c_lat.data_ptr(), out.data_ptr(), lse.data_ptr() if return_lse else None,
+                      B, n_h, Nq, Nk, d_c, causal, window, scale, _dtype_code(q_lat), workspace.data_ptr(),
+                      workspace.numel(), _stream_handle(q_lat.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_mla")
     return out, (lse if return_lse else None)
 
 

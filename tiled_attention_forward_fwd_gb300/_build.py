@@ -12,8 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libattn.so")
 SOURCES = ["attn_api.cu"]
-DEPS = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_bwd_sm103.cuh", "attn_decode.cuh", "attn_short.cuh",
-        "sm103_ptx.cuh", "fastdiv.h"]
+DEPS = ["attn_api.cu", "attn_fwd_sm103.cuh", "attn_bwd_sm103.cuh", "attn_decode.cuh", "attn_mla.cuh",
+        "attn_short.cuh", "sm103_ptx.cuh", "fastdiv.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 _lock = threading.Lock()
 

@@ -71,6 +71,9 @@ def shape_bytes(s, with_lse: bool = True) -> int:
         # reads Q, O, dO and K, V; writes dQ and dK, dV; reads the LSE
         b = 2 * s.d * (4 * s.B * s.Hq * s.Nq + 4 * s.B * s.Hkv * s.Nk)
         return b + (4 * s.B * s.Hq * s.Nq if with_lse else 0)
+    if getattr(s, "mla", False):  # latent attention: one latent cache (B, Nk, d_c) serves as K and V
+        b = 2 * s.d * (2 * s.B * s.Hq * s.Nq + s.B * s.Nk)
+        return b + (4 * s.B * s.Hq * s.Nq if with_lse else 0)
     if getattr(s, "kv_int8", False):  # Q and O 16-bit, K and V one byte per element
         b = 2 * s.d * 2 * s.B * s.Hq * s.Nq + s.d * 2 * s.B * s.Hkv * s.Nk
         return b + (4 * s.B * s.Hq * s.Nq if with_lse else 0)

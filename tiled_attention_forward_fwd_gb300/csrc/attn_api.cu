@@ -16,6 +16,7 @@
 
 #include "../../include/attn.h"
 #include "attn_decode.cuh"
+#include "attn_mla.cuh"
 #include "attn_short.cuh"
 #include "attn_bwd_sm103.cuh"
 #include "attn_fwd_sm103.cuh"
@@ -417,6 +418,89 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   const long long blocks = std::min<long long>((n4 + 255) / 256, 8LL * sms);
   if (launch_pdl(attn_bwd_dq_kernel<BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
                  static_cast<const float *>(p.dq_acc), dQ, n4, s.sm_scale) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- latent (MLA) decode
+struct MlaPlan {
+  int nchunks = 0, chunk_keys = 0, row_blocks = 0;
+  size_t bytes = 0;  // 0: invalid sizes
+};
+
+// Chunks per (request, 16-row block), minimising (waves of one CTA per SM)
+// x (tiles per CTA + 2), as for the split-KV decode.
+static MlaPlan mla_plan(int B, int n_h, int Nq, int Nk, int sms) {
+  MlaPlan pl;
+  if (B <= 0 || n_h <= 0 || Nq <= 0 || Nk <= 0 || sms <= 0) return pl;
+  const long long R = static_cast<long long>(n_h) * Nq;
+  const long long rb = (R + kMlaRows - 1) / kMlaRows;
+  const long long units = static_cast<long long>(B) * rb;
+  if (units > 65535 || R > 0x7fffffffLL / 4) return pl;
+  const long long tiles = (Nk + kDecKeys - 1) / kDecKeys;
+  const long long max_n = std::min<long long>(std::min<long long>(tiles, kDecMaxChunks), 4LL * sms / units + 1);
+  long long best_n = 1, best_cost = -1;
+  for (long long n = 1; n <= max_n; ++n) {
+    const long long cost = ((units * n + sms - 1) / sms) * ((tiles + n - 1) / n + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_n = n;
+    }
+  }
+  int ck = static_cast<int>((Nk + best_n - 1) / best_n);
+  ck = ((ck + kDecKeys - 1) / kDecKeys) * kDecKeys;
+  pl.nchunks = (Nk + ck - 1) / ck;
+  pl.chunk_keys = ck;
+  pl.row_blocks = static_cast<int>(rb);
+  pl.bytes = static_cast<size_t>(B) * R * pl.nchunks * (kMlaD + 1) * sizeof(float);
+  return pl;
+}
+
+template <bool BF16>
+static attn_status_t launch_mla(const void *Q, const void *Cl, void *O, float *LSE, const Shape &s,
+                                const MlaPlan &pl, float *ws, cudaStream_t stream) {
+  MlaParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_map(&p.tmC, Cl, kMlaD, s.Nk, s.B, BF16, kDecKeys)) return ATTN_ERR_CUDA;
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  const long long R = static_cast<long long>(s.Hq) * s.Nq;
+  p.Q = Q;
+  p.ws = ws;
+  p.ws_lse = ws + static_cast<size_t>(s.B) * R * pl.nchunks * kMlaD;
+  p.status = status;
+  p.B = s.B;
+  p.n_h = s.Hq;
+  p.Nq = s.Nq;
+  p.Nk = s.Nk;
+  p.R = static_cast<int>(R);
+  p.row_blocks = pl.row_blocks;
+  p.causal = s.causal ? 1 : 0;
+  p.window = s.window;
+  p.nchunks = pl.nchunks;
+  p.chunk_keys = pl.chunk_keys;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  p.timeout_ns = g_timeout_ns.load();
+  p.stall_after = g_stall_after.load();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  static std::once_flag once[64];
+  static bool ready[64];
+  std::call_once(once[dev], [&] {
+    ready[dev] = cudaFuncSetAttribute(attn_mla_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      MlaCfg::kSmemBytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(attn_mla_kernel<!BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      MlaCfg::kSmemBytes) == cudaSuccess;
+  });
+  if (!ready[dev]) return ATTN_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(static_cast<long long>(s.B) * pl.row_blocks));
+  if (launch_pdl(attn_mla_kernel<BF16>, grid, dim3(kMlaThreads), MlaCfg::kSmemBytes, stream, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const long long rows = static_cast<long long>(s.B) * R;
+  const size_t merge_smem = static_cast<size_t>(((pl.nchunks + 3) & ~3) + kMlaD) * sizeof(float);
+  const float *ws_c = ws, *ws_lse_c = p.ws_lse;
+  if (launch_pdl(attn_decode_combine_kernel<kMlaD, BF16>, dim3(static_cast<unsigned>(rows)), dim3(128), merge_smem,
+                 stream, ws_c, ws_lse_c, O, LSE, static_cast<int>(rows), pl.nchunks) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -845,6 +929,27 @@ attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *
                 : launch_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream);
   return bf16 ? launch_bwd<128, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream)
               : launch_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, s, workspace, stream);
+}
+
+size_t attn_fwd_mla_workspace_bytes(int B, int n_h, int Nq, int Nk, int d_c) {
+  if (d_c != kMlaD) return 0;
+  return mla_plan(B, n_h, Nq, Nk, device_sm_count()).bytes;
+}
+
+attn_status_t attn_fwd_mla(const void *Q_lat, const void *C_lat, void *O_lat, float *LSE, int B, int n_h, int Nq,
+                           int Nk, int d_c, int causal, int window, float sm_scale, attn_dtype_t dtype,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (d_c != kMlaD) return d_c > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  Shape s{B, n_h, 1, Nq, Nk, 128, causal, window, sm_scale, dtype};  // d only passes the checks
+  attn_status_t st = validate(Q_lat, C_lat, C_lat, O_lat, LSE, s);
+  if (st != ATTN_OK) return st;
+  if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  const MlaPlan pl = mla_plan(B, n_h, Nq, Nk, device_sm_count());
+  if (pl.bytes == 0) return ATTN_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  float *ws = static_cast<float *>(workspace);
+  return dtype == ATTN_DTYPE_BF16 ? launch_mla<true>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream)
+                                  : launch_mla<false>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream);
 }
 
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {

@@ -679,7 +679,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, RB, kQuant>::kMinCtas)
 // LSE = lse * ln 2 with lse = log2 sum_c 2^(lse_c).  One CTA of 128 threads
 // per row: the chunk weights go to shared memory, then D/4 threads per chunk
 // row read four columns each (float4) and the 128 / (D/4) groups of chunks
-// are summed in a fixed order.
+// are summed in a fixed order.  D is 64 or 128, or 512 for the latent rows
+// of attn_mla.cuh (then the 128 threads are one group of four columns each).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const float *ws, const float *ws_lse, void *O,
                                                                   float *lse, int rows, int nchunks) {
@@ -731,8 +732,7 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const float *w
   float *part = wts + ((nchunks + 3) & ~3);  // 16-byte aligned
   *reinterpret_cast<float4 *>(part + grp * D + col) = acc;
   __syncthreads();
-  if (tid < D / 2) {
-    const int c2 = tid * 2;
+  for (int c2 = tid * 2; c2 < D; c2 += 256) {  // two columns per thread and pass (D up to 512)
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
