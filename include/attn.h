@@ -299,15 +299,19 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq, int d);
  * workspace (DEVICE, required, 16-byte aligned): at least
  *   attn_fwd_mla_workspace_bytes(...) bytes; the partial results of the key
  *   chunks, fully overwritten by every call (no initialisation needed).
- * Pointers 16-byte aligned, else ATTN_ERR_INVALID_ARG.  Two launches on
- * `stream` (the split kernel, then the merge); nothing is allocated; the call
- * does not synchronise. */
+ * Pointers 16-byte aligned, else ATTN_ERR_INVALID_ARG.  With at least 17
+ * query rows per request (n_h * Nq) the tensor-core kernel runs (pairs of
+ * CTAs, one per half of the 512 output columns, per 128 rows and key
+ * chunk), otherwise a warp-MMA kernel; either is followed by the merge
+ * kernel when the keys are split into more than one chunk.  Enqueued on
+ * `stream`; nothing is allocated; the call does not synchronise. */
 attn_status_t attn_fwd_mla(const void *Q_lat, const void *C_lat, void *O_lat, float *LSE, int B, int n_h, int Nq,
                            int Nk, int d_c, int causal, int window, float sm_scale, attn_dtype_t dtype,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes attn_fwd_mla wants for these sizes on the current device;
- * 0 when the sizes are invalid or d_c is not 512.  No device work. */
+/* Workspace bytes attn_fwd_mla wants for these sizes on the current device
+ * (at least 256); 0 when the sizes are invalid or d_c is not 512.  No
+ * device work. */
 size_t attn_fwd_mla_workspace_bytes(int B, int n_h, int Nq, int Nk, int d_c);
 
 /* End-to-end call on HOST buffers: copies Q, K, V (HOST, ideally pinned) into

@@ -52,14 +52,25 @@ def mla(B, n_h, Nq, Nk, dtype="bf16", causal=True, window=0, scale=1.0 / np.sqrt
 
 @pytest.mark.parametrize("Nk", [1, 2, 63, 64, 65, 200, 1000, 4097])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_ragged_keys(attn, oracle_mod, Nk, dtype):
-    check(attn, oracle_mod, mla(2, 16, 1, Nk, dtype), 170, Nk)
+@pytest.mark.parametrize("n_h", [16, 128])  # 16 rows: warp-MMA kernel; 128: tensor-core kernel
+def test_ragged_keys(attn, oracle_mod, Nk, dtype, n_h):
+    check(attn, oracle_mod, mla(2, n_h, 1, Nk, dtype), 170, Nk + n_h)
+
+
+@pytest.mark.parametrize("B,Nk", [(76, 500), (40, 200)])
+def test_one_chunk_direct_output(attn, oracle_mod, B, Nk):
+    """Enough requests to fill the GPU with one key chunk each: the tensor-core
+    kernel writes O and LSE itself (no workspace partials, no merge)."""
+    s = mla(B, 128, 1, Nk)
+    assert attn.attn_fwd_mla_workspace_bytes(B, 128, 1, Nk, 512) == 256  # no partials
+    check(attn, oracle_mod, s, 176, B)
 
 
 @pytest.mark.parametrize("B,n_h,Nq", [(1, 128, 1), (2, 8, 3), (1, 4, 1), (3, 20, 1), (1, 128, 4), (2, 1, 7)])
 @pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 300)])
 def test_heads_and_queries(attn, oracle_mod, B, n_h, Nq, causal, window):
-    """Row blocks of 16 over n_h x Nq rows (ragged last block), masks."""
+    """Rows n_h x Nq per request on both kernels (16-row blocks below 17 rows,
+    128-row blocks from there; ragged last blocks), masks."""
     check(attn, oracle_mod, mla(B, n_h, Nq, 1500, "bf16", causal, window), 171, B * 100 + n_h + Nq)
 
 
@@ -149,3 +160,29 @@ def test_argument_errors(attn):
     assert attn.attn_fwd_mla_workspace_bytes(1, 4, 1, 100, 256) == 0
     torch.cuda.synchronize()
     assert attn.device_status() == attn.ATTN_OK
+
+
+# (requests, heads, tiles loaded before the stall): enough requests that each
+# CTA holds one chunk of all 16 tiles (so that it stalls mid-chunk)
+STALLS = [(152, 16, 0), (152, 16, 1), (40, 128, 0), (40, 128, 1), (40, 128, 3)]
+
+
+@pytest.mark.parametrize("B,n_h,stall", STALLS)
+def test_stalled_producer_times_out(attn, oracle_mod, B, n_h, stall):
+    """The producer stops loading after `stall` latent tiles: the roles waiting
+    for the next one run into the wait limit, the call comes back with
+    ATTN_ERR_TIMEOUT, and the next call on the same buffers is right."""
+    s = mla(B, n_h, 1, 1000)
+    q, c4 = latent_inputs(s, 177)
+    qd, cd = q.cuda(), c4[:, 0].cuda()
+    try:
+        attn.attn_set_wait_timeout_ns(200_000)
+        attn.attn_set_test_stall(stall)
+        attn.flash_attn_mla(qd, cd, causal=True, sm_scale=s.scale)
+        assert attn.device_status() == attn.ATTN_ERR_TIMEOUT
+        assert attn.device_status() == attn.ATTN_OK  # read and cleared
+    finally:
+        attn.attn_set_wait_timeout_ns(0)
+        attn.attn_set_test_stall(-1)
+    o, lse = run(attn, s, q, c4)
+    pu.check_full(s, q, c4, c4, o, lse, oracle_mod, "after a stall")

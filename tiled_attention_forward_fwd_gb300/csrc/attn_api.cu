@@ -505,6 +505,95 @@ static attn_status_t launch_mla(const void *Q, const void *Cl, void *O, float *L
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Tensor-core latent attention: CTA pairs (one per output half) per
+// (request, 128-row block, key chunk), one CTA per SM.  Chunks minimise
+// waves x (tiles per chunk + 2, + 4 for the partials' round trip through the
+// workspace when there is more than one chunk).
+static MlaPlan mla_tc_plan(int B, int n_h, int Nq, int Nk, int sms) {
+  MlaPlan pl;
+  if (B <= 0 || n_h <= 0 || Nq <= 0 || Nk <= 0 || sms <= 0) return pl;
+  const long long R = static_cast<long long>(n_h) * Nq;
+  const long long rb = (R + kMlaTcRows - 1) / kMlaTcRows;
+  const long long units = static_cast<long long>(B) * rb;
+  if (units > 65535 || R > 0x7fffffffLL / 4) return pl;
+  const long long tiles = (Nk + kMlaTcKeys - 1) / kMlaTcKeys;
+  const long long max_n = std::min<long long>(std::min<long long>(tiles, kDecMaxChunks), 4LL * sms / (2 * units) + 1);
+  long long best_n = 1, best_cost = -1;
+  for (long long n = 1; n <= max_n; ++n) {
+    const long long waves = (2 * units * n + sms - 1) / sms;
+    const long long cost = waves * ((tiles + n - 1) / n + 2 + (n > 1 ? 4 : 0));
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_n = n;
+    }
+  }
+  int ck = static_cast<int>((Nk + best_n - 1) / best_n);
+  ck = ((ck + kMlaTcKeys - 1) / kMlaTcKeys) * kMlaTcKeys;
+  pl.nchunks = (Nk + ck - 1) / ck;
+  pl.chunk_keys = ck;
+  pl.row_blocks = static_cast<int>(rb);
+  pl.bytes = pl.nchunks > 1 ? static_cast<size_t>(B) * R * pl.nchunks * (kMlaD + 1) * sizeof(float) : 0;
+  return pl;
+}
+
+static bool mla_use_tc(int n_h, int Nq) { return static_cast<long long>(n_h) * Nq >= kMlaTcMinRows; }
+
+template <bool BF16>
+static attn_status_t launch_mla_tc(const void *Q, const void *Cl, void *O, float *LSE, const Shape &s,
+                                   const MlaPlan &pl, float *ws, cudaStream_t stream) {
+  MlaTcParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long R = static_cast<long long>(s.Hq) * s.Nq;
+  if (!make_map(&p.tmQ, Q, kMlaD, static_cast<int>(R), s.B, BF16, kMlaTcRows) ||
+      !make_map(&p.tmC, Cl, kMlaD, s.Nk, s.B, BF16, kMlaTcKeys))
+    return ATTN_ERR_CUDA;
+  int *status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  p.Q = Q;
+  p.O = O;
+  p.lse = LSE;
+  p.ws = ws;
+  p.ws_lse = ws + static_cast<size_t>(s.B) * R * pl.nchunks * kMlaD;
+  p.status = status;
+  p.B = s.B;
+  p.Nq = s.Nq;
+  p.Nk = s.Nk;
+  p.R = static_cast<int>(R);
+  p.row_blocks = pl.row_blocks;
+  p.causal = s.causal ? 1 : 0;
+  p.window = s.window;
+  p.nchunks = pl.nchunks;
+  p.chunk_keys = pl.chunk_keys;
+  p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
+  p.timeout_ns = g_timeout_ns.load();
+  p.stall_after = g_stall_after.load();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  static std::once_flag once[64];
+  static bool ready[64];
+  std::call_once(once[dev], [&] {
+    ready[dev] = cudaFuncSetAttribute(attn_mla_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      MlaTcCfg::kSmemBytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(attn_mla_tc_kernel<!BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      MlaTcCfg::kSmemBytes) == cudaSuccess;
+  });
+  if (!ready[dev]) return ATTN_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(2 * pl.nchunks),
+                  static_cast<unsigned>(static_cast<long long>(s.B) * pl.row_blocks));
+  if (launch_pdl(attn_mla_tc_kernel<BF16>, grid, dim3(kMlaTcThreads), MlaTcCfg::kSmemBytes, stream, p) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (pl.nchunks > 1) {
+    const long long rows = static_cast<long long>(s.B) * R;
+    const size_t merge_smem = static_cast<size_t>(((pl.nchunks + 3) & ~3) + kMlaD) * sizeof(float);
+    const float *ws_c = ws, *ws_lse_c = p.ws_lse;
+    if (launch_pdl(attn_decode_combine_kernel<kMlaD, BF16>, dim3(static_cast<unsigned>(rows)), dim3(128),
+                   merge_smem, stream, ws_c, ws_lse_c, O, LSE, static_cast<int>(rows), pl.nchunks) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- split-KV (decode) path
 struct DecPlan {
   int nchunks = 0, chunk_keys = 0;
@@ -932,8 +1021,11 @@ attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *
 }
 
 size_t attn_fwd_mla_workspace_bytes(int B, int n_h, int Nq, int Nk, int d_c) {
-  if (d_c != kMlaD) return 0;
-  return mla_plan(B, n_h, Nq, Nk, device_sm_count()).bytes;
+  if (d_c != kMlaD || B <= 0 || n_h <= 0 || Nq <= 0 || Nk <= 0) return 0;
+  const int sms = device_sm_count();
+  const MlaPlan pl = mla_use_tc(n_h, Nq) ? mla_tc_plan(B, n_h, Nq, Nk, sms) : mla_plan(B, n_h, Nq, Nk, sms);
+  if (pl.nchunks == 0) return 0;
+  return std::max<size_t>(pl.bytes, 256);
 }
 
 attn_status_t attn_fwd_mla(const void *Q_lat, const void *C_lat, void *O_lat, float *LSE, int B, int n_h, int Nq,
@@ -944,12 +1036,19 @@ attn_status_t attn_fwd_mla(const void *Q_lat, const void *C_lat, void *O_lat, fl
   attn_status_t st = validate(Q_lat, C_lat, C_lat, O_lat, LSE, s);
   if (st != ATTN_OK) return st;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
-  const MlaPlan pl = mla_plan(B, n_h, Nq, Nk, device_sm_count());
-  if (pl.bytes == 0) return ATTN_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  const int sms = device_sm_count();
+  const bool tc = mla_use_tc(n_h, Nq);
+  const MlaPlan pl = tc ? mla_tc_plan(B, n_h, Nq, Nk, sms) : mla_plan(B, n_h, Nq, Nk, sms);
+  if (pl.nchunks == 0) return ATTN_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < std::max<size_t>(pl.bytes, 256) || !aligned16(workspace))
+    return ATTN_ERR_INVALID_ARG;
   float *ws = static_cast<float *>(workspace);
-  return dtype == ATTN_DTYPE_BF16 ? launch_mla<true>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream)
-                                  : launch_mla<false>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream);
+  const bool bf = dtype == ATTN_DTYPE_BF16;
+  if (tc)
+    return bf ? launch_mla_tc<true>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream)
+              : launch_mla_tc<false>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream);
+  return bf ? launch_mla<true>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream)
+            : launch_mla<false>(Q_lat, C_lat, O_lat, LSE, s, pl, ws, stream);
 }
 
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {

@@ -294,4 +294,449 @@ __global__ void __launch_bounds__(kMlaThreads, 1) attn_mla_kernel(const __grid_c
   }
 }
 
+// ============================================================================
+// The same attention on the 5th-generation tensor cores, for requests with
+// more than a few query rows (n_h x Nq; 128 for one query of DeepSeek-V2's
+// 128 heads).
+//
+// A CTA takes 128 query rows of one request, one chunk of its keys, and one
+// half of the 512 output columns: two CTAs (adjacent in the grid, so they
+// read the same latent tiles at the same time and the second read hits L2)
+// share a row block and a chunk.  Each computes the full scores S = Q~ C^T
+// (128 x 64 keys per tile, K = 512), its own softmax (both compute the same
+// S bit for bit: the same MMAs in the same order), and O_half += P C_half
+// (N = 256).  Tensor memory (512 columns) holds O_half (256), the half of
+// Q~ whose columns the CTA does not output (128 columns of packed pairs:
+// the A operand of half of the score MMAs) and two S buffers (64 each; P is
+// written over S as 16-bit pairs and read from there by the P V MMA).  The
+// other half of Q~ sits in shared memory (64 KB): with all of Q~ read from
+// shared memory for every tile, the score MMAs would need more operand
+// bandwidth than shared memory gives at N = 64.
+//
+// Latent tiles (64 keys) arrive as two halves of 256 columns (32 KB each,
+// four 128B-swizzled boxes): the half this CTA outputs ("own", kept until
+// its P V has run: a 3-slot ring) and the other half ("other", needed only
+// by the score MMAs: a 2-slot ring, released as soon as they complete).
+//
+// Roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (one lane)
+// and TMEM owner, warps 2-5 softmax (one query row per thread; warp w reads
+// TMEM lanes 32 (w % 4) ..).  Pipeline per tile i: S(i) is issued before
+// P V(i-1), so the softmax of tile i overlaps the P V of tile i-1; S(i)
+// reuses the buffer of P(i-2), whose P V was issued before it (the tensor
+// pipe completes one CTA's MMAs in order).
+constexpr int kMlaTcRows = 128;
+constexpr int kMlaTcKeys = 64;
+constexpr int kMlaTcThreads = 192;
+constexpr int kMlaTcMinRows = 17;  // query rows per request from which this kernel is used
+
+struct MlaTcCfg {
+  static constexpr int kOwnSlots = 3, kOthSlots = 2;
+  static constexpr int kBoxBytes = kMlaTcKeys * 128;      // 64 keys x 64 columns x 2 bytes
+  static constexpr int kHalfBytes = 4 * kBoxBytes;         // 64 keys x 256 columns: 32 KB
+  static constexpr int kQBoxBytes = kMlaTcRows * 128;      // 128 rows x 64 columns: 16 KB
+  static constexpr int kOffQ = 0;                          // the own half of Q~: four boxes
+  static constexpr int kOffOwn = kOffQ + 4 * kQBoxBytes;
+  static constexpr int kOffOth = kOffOwn + kOwnSlots * kHalfBytes;
+  static constexpr int kOffBar = kOffOth + kOthSlots * kHalfBytes;
+  // barriers: own full/empty [3], other full/empty [2], Q, S full [2], P V done, O final, drain
+  static constexpr int kNumBars = 2 * kOwnSlots + 2 * kOthSlots + 1 + 2 + 3;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, TMEM slot, abort flag; alignment
+  static_assert(kNumBars * 8 + 8 <= 256, "barriers fit");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // TMEM columns
+  static constexpr uint32_t kColO = 0, kColQt = 256, kColS = 384, kTmemCols = 512;
+};
+
+struct MlaTcParams {
+  CUtensorMap tmQ;  // (512, R, B), box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tmC;  // (512, Nk, B), box 64 x 64 x 1, 128B swizzle
+  const void *Q;    // (B, R, 512): the TMEM half is loaded by the softmax threads
+  void *O;          // direct output (nchunks == 1): (B, R, 512) 16-bit
+  float *lse;       // direct output: (B, R) natural log, or null
+  float *ws;        // nchunks > 1: [B*R][nchunks][512] normalised partials
+  float *ws_lse;    // nchunks > 1: [B*R][nchunks] log2 LSE
+  int *status;
+  int B, Nq, Nk, R, row_blocks;
+  int causal, window;
+  int nchunks, chunk_keys;
+  float scale_log2;
+  unsigned long long timeout_ns;
+  int stall_after;
+};
+
+enum MlaError : int { kErrMlaWait = 0x401 };
+
+// Named barriers between the softmax warps (128, arrive) and the MMA warp
+// (32, sync): P(i) written; the TMEM half of Q~ written.
+constexpr uint32_t kBarMlaP = 1, kBarMlaQt = 2, kBarMlaThreads = 160;
+
+// Four score MMAs of K = 16 with A from TMEM (column a + 8k) and a K-major B
+// (descriptor b + 2k: 32 bytes further in the swizzle row); the first
+// accumulates iff `accumulate` != 0.
+__device__ __forceinline__ void umma_ts_x4_kmajor(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, p1;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 p1, %4, %4;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, p1;\n\t}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Four P V MMAs of K = 16 keys: P at TMEM column a + 8k, B MN-major
+// (descriptor b + 128k: 16 key rows = 2048 bytes further).
+__device__ __forceinline__ void umma_ts_x4_mnmajor(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, p1;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 p1, %4, %4;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, p1;\n\t}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kMlaTcThreads, 1) attn_mla_tc_kernel(const __grid_constant__ MlaTcParams p) {
+  using C = MlaTcCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ), sOwn = smem_u32(smem + C::kOffOwn);
+  const uint32_t sOth = smem_u32(smem + C::kOffOth);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bOwnFull = [&](int s) { return bar0 + 8u * s; };
+  auto bOwnEmpty = [&](int s) { return bar0 + 8u * (C::kOwnSlots + s); };
+  auto bOthFull = [&](int s) { return bar0 + 8u * (2 * C::kOwnSlots + s); };
+  auto bOthEmpty = [&](int s) { return bar0 + 8u * (2 * C::kOwnSlots + C::kOthSlots + s); };
+  const uint32_t bX = bar0 + 8u * (2 * C::kOwnSlots + 2 * C::kOthSlots);
+  const uint32_t bQ = bX;
+  auto bSfull = [&](int t) { return bX + 8u * (1 + t); };
+  const uint32_t bPVdone = bX + 24, bOfinal = bX + 32, bDrain = bX + 40;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x & 1, chunk = blockIdx.x >> 1;
+  const int b = blockIdx.y / p.row_blocks, rblk = blockIdx.y - b * p.row_blocks;
+  WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+  pdl_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::kOwnSlots; ++s) {
+      mbar_init(bOwnFull(s), 1);
+      mbar_init(bOwnEmpty(s), 1);
+    }
+    for (int s = 0; s < C::kOthSlots; ++s) {
+      mbar_init(bOthFull(s), 1);
+      mbar_init(bOthEmpty(s), 1);
+    }
+    mbar_init(bQ, 1);
+    mbar_init(bSfull(0), 1);
+    mbar_init(bSfull(1), 1);
+    mbar_init(bPVdone, 1);
+    mbar_init(bOfinal, 1);
+    mbar_init(bDrain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && elect_one()) {
+    tma_prefetch_desc(&p.tmQ);
+    tma_prefetch_desc(&p.tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  const uint32_t tmem = *tmem_slot;
+  const int k0 = chunk * p.chunk_keys;
+  const int k1 = min(k0 + p.chunk_keys, p.Nk);
+  const int ntiles = (k1 - k0 + kMlaTcKeys - 1) / kMlaTcKeys;  // >= 1: every chunk holds keys
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    bool ok = true;
+    if (elect_one()) {
+      mbar_arrive_expect_tx(bQ, 4 * C::kQBoxBytes);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tma_load_3d(sQ + c * C::kQBoxBytes, &p.tmQ, bQ, h * 256 + c * 64, rblk * kMlaTcRows, b);
+    }
+    __syncwarp();
+    int nown = 0, noth = 0;  // halves issued
+    for (int i = 0; ok && i < ntiles; ++i) {
+      if (p.stall_after >= 0 && i >= p.stall_after) {  // test hook: stop loading
+        ok = false;
+        break;
+      }
+      // columns 0-255 first: the score MMAs run over the columns in order
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        const bool own = part == h;
+        uint32_t dst, full;
+        if (own) {
+          const int s = i % C::kOwnSlots;
+          if (i >= C::kOwnSlots && !mbar_wait_warp(bOwnEmpty(s), ((i / C::kOwnSlots) - 1) & 1, wc, kErrMlaWait)) {
+            ok = false;
+            break;
+          }
+          dst = sOwn + s * C::kHalfBytes;
+          full = bOwnFull(s);
+        } else {
+          const int s = i % C::kOthSlots;
+          if (i >= C::kOthSlots && !mbar_wait_warp(bOthEmpty(s), ((i / C::kOthSlots) - 1) & 1, wc, kErrMlaWait)) {
+            ok = false;
+            break;
+          }
+          dst = sOth + s * C::kHalfBytes;
+          full = bOthFull(s);
+        }
+        if (elect_one()) {
+          mbar_arrive_expect_tx(full, C::kHalfBytes);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tma_load_3d(dst + c * C::kBoxBytes, &p.tmC, full, part * 256 + c * 64, k0 + i * kMlaTcKeys, b);
+        }
+        __syncwarp();
+        if (own) nown = i + 1;
+        else noth = i + 1;
+      }
+    }
+    if (lane == 0) {  // never leave with a copy of ours in flight
+      mbar_drain_dec(bQ, 0);
+      for (int i = max(0, nown - C::kOwnSlots); i < nown; ++i)
+        mbar_drain_dec(bOwnFull(i % C::kOwnSlots), (i / C::kOwnSlots) & 1);
+      for (int i = max(0, noth - C::kOthSlots); i < noth; ++i)
+        mbar_drain_dec(bOthFull(i % C::kOthSlots), (i / C::kOthSlots) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(kMlaTcRows, kMlaTcKeys, BF16, false, false);
+    constexpr uint32_t kIdPV = idesc_f16(kMlaTcRows, 256, BF16, false, true);
+    bool ok = mbar_wait_warp(bQ, 0, wc, kErrMlaWait);
+    named_bar_sync(kBarMlaQt, kBarMlaThreads);  // the TMEM half of Q~ is written
+    // After an abort no MMA is issued, but S full, P V done and O final are
+    // still signalled by plain arrivals: the softmax warps wait for them
+    // without polling the abort flag, and so never run ahead of this warp
+    // at the P barrier.
+    auto issue_s = [&](int i) {
+      const int so = i % C::kOwnSlots, st = i % C::kOthSlots;
+      if (ok) ok = mbar_wait_warp(h == 0 ? bOwnFull(so) : bOthFull(st),
+                                  ((h == 0 ? i / C::kOwnSlots : i / C::kOthSlots)) & 1, wc, kErrMlaWait);
+      if (ok) ok = mbar_wait_warp(h == 0 ? bOthFull(st) : bOwnFull(so),
+                                  ((h == 0 ? i / C::kOthSlots : i / C::kOwnSlots)) & 1, wc, kErrMlaWait);
+      if (!ok) {
+        if (elect_one()) mbar_arrive(bSfull(i & 1));
+        __syncwarp();
+        return;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t d = tmem + C::kColS + (i & 1) * kMlaTcKeys;
+        const uint32_t own_half = sOwn + so * C::kHalfBytes, oth_half = sOth + st * C::kHalfBytes;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t acc = (part | c) ? 1u : 0u;
+            if (part == h) {  // own columns: A = Q~ from shared memory
+              const uint64_t ad = sdesc_sw128(sQ + c * C::kQBoxBytes, 16, 1024);
+              const uint64_t bd = sdesc_sw128(own_half + c * C::kBoxBytes, 16, 1024);
+              umma_ss_x4(d, ad, bd, kIdS, acc);
+            } else {  // other columns: A = Q~ from TMEM (8 columns per 16 values)
+              const uint64_t bd = sdesc_sw128(oth_half + c * C::kBoxBytes, 16, 1024);
+              umma_ts_x4_kmajor(d, tmem + C::kColQt + c * 32, bd, kIdS, acc);
+            }
+          }
+        }
+        umma_commit(bOthEmpty(st));  // the other half has served its only use
+        umma_commit(bSfull(i & 1));
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int j, bool last) {
+      named_bar_sync(kBarMlaP, kBarMlaThreads);  // P(j) written (and O rescaled)
+      ok = ok && !__any_sync(0xffffffffu, *reinterpret_cast<volatile int *>(abort_flag) != 0);
+      if (!ok) {
+        if (elect_one()) {
+          mbar_arrive(bPVdone);
+          if (last) mbar_arrive(bOfinal);
+        }
+        __syncwarp();
+        return;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        const int so = j % C::kOwnSlots;
+        const uint64_t vd = sdesc_sw128(sOwn + so * C::kHalfBytes, C::kBoxBytes, 1024);
+        umma_ts_x4_mnmajor(tmem + C::kColO, tmem + C::kColS + (j & 1) * kMlaTcKeys, vd, kIdPV, j > 0 ? 1u : 0u);
+        umma_commit(bOwnEmpty(so));
+        umma_commit(bPVdone);
+        if (last) umma_commit(bOfinal);
+      }
+      __syncwarp();
+    };
+    for (int i = 0; i < ntiles; ++i) {
+      issue_s(i);
+      if (i > 0) issue_pv(i - 1, false);
+    }
+    issue_pv(ntiles - 1, true);
+    // every MMA of this warp completes before TMEM is released
+    if (elect_one()) {
+      umma_commit(bDrain);
+      mbar_drain_dec(bDrain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ softmax (one row per thread)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int qr = rblk * kMlaTcRows + row;
+    const bool live_row = qr < p.R;
+    const int pos = p.Nk - p.Nq + (qr % p.Nq);  // row qr is query qr % Nq of head qr / Nq
+    // the half of Q~ this CTA does not output -> TMEM, as packed pairs
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.Q) +
+                                                         (static_cast<size_t>(b) * p.R + (live_row ? qr : 0)) * kMlaD +
+                                                         (1 - h) * 256);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = live_row ? __ldg(src + cc * 8 + j) : make_uint4(0, 0, 0, 0);
+          v[4 * j] = w.x;
+          v[4 * j + 1] = w.y;
+          v[4 * j + 2] = w.z;
+          v[4 * j + 3] = w.w;
+        }
+        tmem_st32(tmem + lane_off + C::kColQt + cc * 32, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_arrive(kBarMlaQt, kBarMlaThreads);
+    }
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    // live keys of this row: one interval [lo, hi)
+    const int hi = min(k1, p.causal ? pos + 1 : k1);
+    const int lo = (p.window > 0) ? pos - p.window + 1 : k0;
+    for (int i = 0; i < ntiles; ++i) {
+      ok = mbar_wait_signal(bSfull(i & 1), (i >> 1) & 1, wc, kErrMlaWait) && ok;
+      const uint32_t scol = tmem + lane_off + C::kColS + (i & 1) * kMlaTcKeys;
+      uint32_t sr[kMlaTcKeys];
+      tc_fence_after();
+      tmem_ld64(scol, sr);
+      const int key0 = k0 + i * kMlaTcKeys;
+      if (key0 + kMlaTcKeys > hi || key0 < lo) {
+#pragma unroll
+        for (int c = 0; c < kMlaTcKeys; ++c)
+          if (key0 + c >= hi || key0 + c < lo) sr[c] = 0xff800000u;  // -inf
+      }
+      float mx = __uint_as_float(sr[0]);
+#pragma unroll
+      for (int c = 1; c < kMlaTcKeys; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      const float m_new = fmaxf(m, mx * sl2);
+      const bool first = i == 0;
+      const bool rescale = !first && __any_sync(0xffffffffu, m_new > m + kMlaRescale);
+      float alpha = 1.f;
+      if (first || rescale) {
+        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+        m = m_new;
+      }
+      if (rescale) {
+        // O holds tiles up to i-1: wait for P V(i-1) (P V(i-2) completed
+        // before S(i), so this phase is the only one that can be open)
+        ok = mbar_wait_signal(bPVdone, (i - 1) & 1, wc, kErrMlaWait) && ok;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + C::kColO + cc * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(tmem + lane_off + C::kColO + cc * 32, r);
+        }
+      }
+      const float negm = (m == -INFINITY) ? 0.f : -m;
+      uint32_t pk[kMlaTcKeys / 2];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMlaTcKeys / 2; ++c) {
+        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, negm));
+        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, negm));
+        pk[c] = pack2<BF16>(e0, e1);
+        sum0 += e0;
+        sum1 += e1;
+      }
+      tmem_st32(scol, pk);  // P over the first 32 columns of this S buffer
+      l = first ? (sum0 + sum1) : l * alpha + (sum0 + sum1);
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_arrive(kBarMlaP, kBarMlaThreads);
+    }
+    // ---- epilogue: O_half / l and the LSE
+    ok = mbar_wait_signal(bOfinal, 0, wc, kErrMlaWait) && ok;
+    tc_fence_after();
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const size_t grow = static_cast<size_t>(b) * p.R + (live_row ? qr : 0);
+    if (ok) {
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::kColO + cc * 32, r);
+        if (!live_row) continue;
+        const int col = h * 256 + cc * 32;
+        if (p.nchunks == 1) {
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.O) + grow * kMlaD + col);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2<BF16>(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+            w.y = pack2<BF16>(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+            w.z = pack2<BF16>(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+            w.w = pack2<BF16>(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+            dst[q] = w;
+          }
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(p.ws + (grow * p.nchunks + chunk) * kMlaD + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                 __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        }
+      }
+      if (live_row && h == 0) {
+        const float lse2 = (l > 0.f) ? m + log2f(l) : -INFINITY;
+        if (p.nchunks == 1) {
+          if (p.lse != nullptr) p.lse[grow] = lse2 * 0.69314718055994530942f;
+        } else {
+          p.ws_lse[grow * p.nchunks + chunk] = lse2;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
 }  // namespace attn
