@@ -85,6 +85,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--per-call", action="store_true", help="print per-call timings to stderr")
+    ap.add_argument("--launch-floor", action="store_true",
+                    help="only time empty-kernel CUDA graphs (the fixed cost of a launch) and print them")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed replays after the warm-up, before the timed steps")
     return ap.parse_args()
@@ -702,10 +704,50 @@ def reference_arm(args):
 
 
 # ---------------------------------------------------------------- main
+def launch_floor(device) -> dict:
+    """Device time, between two events captured around it in a CUDA graph (as
+    bench.py times one call), of one empty kernel launched like the
+    library's kernels, for a few grid / shared-memory sizes, and of two of
+    them back to back: the fixed cost that a call of one or two launches
+    cannot go below."""
+    import tiled_attention_forward_fwd_gb300 as attn
+
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    out = {}
+    for grid, smem, n in ((1, 0, 1), (152, 0, 1), (608, 0, 1), (152, 200 * 1024, 1), (608, 100 * 1024, 1),
+                          (608, 100 * 1024, 2)):
+        e0, e1 = make_event(), make_event()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e0.record(torch.cuda.current_stream())
+            for _ in range(n):
+                st = attn.attn_empty_launch(grid, 160, smem, torch.cuda.current_stream().cuda_stream)
+                if st != attn.ATTN_OK:
+                    raise RuntimeError(attn.attn_status_string(st))
+            e1.record(torch.cuda.current_stream())
+        times = []
+        for k in range(60):
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+                g.replay()
+            stream.synchronize()
+            if k >= 10:
+                times.append(e0.elapsed_time(e1) * 1e3)
+        out[f"grid{grid}_smem{smem // 1024}KB_x{n}"] = float(np.median(times))
+    return out
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.launch_floor:
+        device = torch.device("cuda", 0)
+        torch.cuda.set_device(device)
+        print(json.dumps({"launch_floor_us_per_graph": launch_floor(device),
+                          "note": "median device time between events around empty kernels inside a CUDA graph (160 threads each), as bench.py times a call"}), flush=True)
+        return 0
     ws, rank, local = dist_env()
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
     device = torch.device("cuda", local)

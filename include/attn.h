@@ -353,6 +353,14 @@ const char *attn_status_string(attn_status_t status);
 /* ATTN_ABI_VERSION of the loaded library. */
 int attn_abi_version(void);
 
+/* Measurement aid with no counterpart in the pages: launches an empty kernel
+ * on `stream` the way every kernel here is launched (programmatic dependent
+ * launch, `grid` CTAs of `threads` threads, `smem_bytes` of dynamic shared
+ * memory), so that the fixed cost of a launch in a stream or a CUDA graph can
+ * be measured next to a call.  ATTN_ERR_INVALID_ARG for grid < 1, threads
+ * outside 1..1024 or more than 227 KB of shared memory. */
+attn_status_t attn_empty_launch(int grid, int threads, size_t smem_bytes, cudaStream_t stream);
+
 /* Split-KV decode that allocates nothing: the same computation as attn_fwd_ex
  * with a workspace, but its scratch lives in a fixed array inside the
  * library, so the caller passes only inputs and outputs.  The pages have no

@@ -37,7 +37,7 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
             "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8", "attn_bwd", "attn_bwd_workspace_bytes",
-            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes"]
+            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes", "attn_empty_launch"]
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_mla.restype = ci
         L.attn_fwd_mla_workspace_bytes.argtypes = [ci] * 5
         L.attn_fwd_mla_workspace_bytes.restype = sz
+        L.attn_empty_launch.argtypes = [ci, ci, sz, vp]
+        L.attn_empty_launch.restype = ci
         L.attn_status_string.argtypes = [ci]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_abi_version.argtypes = []
@@ -186,6 +188,10 @@ def attn_fwd_mla(Q_lat, C_lat, O_lat, LSE, B, n_h, Nq, Nk, d_c, causal, window, 
                  workspace_bytes, stream) -> int:
     return lib().attn_fwd_mla(Q_lat, C_lat, O_lat, LSE, B, n_h, Nq, Nk, d_c, int(causal), int(window),
                               float(sm_scale), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def attn_empty_launch(grid, threads, smem_bytes, stream) -> int:
+    return int(lib().attn_empty_launch(int(grid), int(threads), int(smem_bytes), stream))
 
 
 def attn_fwd_mla_workspace_bytes(B, n_h, Nq, Nk, d_c) -> int:

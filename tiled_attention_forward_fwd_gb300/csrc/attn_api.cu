@@ -23,6 +23,13 @@
 
 namespace attn {
 
+// An empty kernel, launched like the others (programmatic dependent launch):
+// the fixed cost of one launch, for measurements.
+__global__ void attn_empty_kernel() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
 // Kernel status word (one per device): first error code wins, 0 = fine.
 __device__ int g_status;
 
@@ -1210,6 +1217,23 @@ const char *attn_status_string(attn_status_t status) {
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+attn_status_t attn_empty_launch(int grid, int threads, size_t smem_bytes, cudaStream_t stream) {
+  if (grid <= 0 || threads <= 0 || threads > 1024 || smem_bytes > 232448) return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  static std::once_flag once[64];
+  static bool ready[64];
+  std::call_once(once[dev], [&] {
+    ready[dev] = cudaFuncSetAttribute(attn::attn_empty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      232448) == cudaSuccess;
+  });
+  if (!ready[dev]) return ATTN_ERR_CUDA;
+  if (attn::launch_pdl(attn::attn_empty_kernel, dim3(static_cast<unsigned>(grid)), dim3(static_cast<unsigned>(threads)),
+                       smem_bytes, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 }  // extern "C"
 
