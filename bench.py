@@ -326,6 +326,8 @@ def prepare(workload: str, device):
         if path == attn.ATTN_PATH_PREFILL_SPLIT and shape.window > 0:
             path = attn.ATTN_PATH_PREFILL  # the split is not used with a window
         split = path in (attn.ATTN_PATH_SPLIT_KV, attn.ATTN_PATH_SPLIT_KV_FUSED, attn.ATTN_PATH_PREFILL_SPLIT)
+        if shape.kv_int8:  # the int8 entry plans its chunks for its own kernel
+            wsb = attn.attn_fwd_kv_int8_workspace_bytes(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nk, shape.d)
         c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device) if split else None
         c["path"] = path
         c["kernel"] = {attn.ATTN_PATH_PREFILL: "attn_fwd_kernel", attn.ATTN_PATH_PREFILL_SPLIT: "attn_fwd_kernel",

@@ -142,13 +142,17 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
 /* The split-KV plan for these sizes on a device of `sms` SMs holding
  * `ctas_per_sm` split CTAs each (the occupancy of the split kernel), without
  * device work (cruxr.ai "FlashDecoding": the keys are cut into chunks that
- * are processed in parallel, then merged).  paged != 0 gives attn_fwd_paged's
- * plan (at most 2048 keys a chunk, max_seq_len = Nk).  info (HOST, 5
- * values, written): chunks per GQA group, keys per chunk (a multiple of 64;
- * the last chunk may be shorter), 1 when each group's last CTA to finish
- * merges (one launch) else 0, byte offset of the per-group arrival counters
- * (8 bytes each) in the workspace, and the workspace bytes.  Returns 0, or -1 when the shape does not take the
- * split-KV path ((Hq / Hkv) * Nq > 32, B * Hkv > 65535, bad sizes). */
+ * are processed in parallel, then merged).  `paged` selects the call:
+ * 0 attn_fwd_ex on a flat 16-bit cache (chunks minimise CTAs per SM x
+ * (tiles per CTA + 6)), 1 attn_fwd_paged (waves of resident CTAs x (tiles
+ * per CTA + 2), then at most 2048 keys a chunk; max_seq_len = Nk), 2
+ * attn_fwd_kv_int8 (the waves model, no cap).  info (HOST, 5 values,
+ * written): chunks per GQA group, keys per chunk (a multiple of 64; the last
+ * chunk may be shorter), 1 when each group's last CTA to finish merges (one
+ * launch) else 0, byte offset of the per-group arrival counters (8 bytes
+ * each) in the workspace, and the workspace bytes.  Returns 0, or -1 when
+ * the shape does not take the split-KV path ((Hq / Hkv) * Nq > 32,
+ * B * Hkv > 65535, bad sizes) or `paged` is not 0, 1 or 2. */
 int attn_fwd_decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int paged, int sms, int ctas_per_sm,
                          long long *info);
 
@@ -242,13 +246,19 @@ int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d);
  * K_codes, V_codes (DEVICE, int8, B x Hkv x Nk x d, dense, 16-byte aligned);
  *   every other argument as attn_fwd_ex.  Only shapes that take the split-KV
  *   path (query groups of at most 32 rows: (Hq / Hkv) * Nq <= 32) are served;
- *   others return ATTN_ERR_UNSUPPORTED.  workspace (DEVICE, required): at
- *   least attn_fwd_workspace_bytes(...) bytes, as for attn_fwd_ex.
+ *   others return ATTN_ERR_UNSUPPORTED.  workspace (DEVICE, required, 16-byte
+ *   aligned): at least attn_fwd_kv_int8_workspace_bytes(...) bytes, laid
+ *   out as attn_fwd_ex's split-KV workspace (its chunk plan differs: two
+ *   resident CTAs per SM pay for the widening work).
  *   k_scale, v_scale: finite and > 0, else ATTN_ERR_INVALID_ARG. */
 attn_status_t attn_fwd_kv_int8(const void *Q, const void *K_codes, const void *V_codes, float k_scale,
                                float v_scale, void *O, float *LSE, int B, int Hq, int Hkv, int Nq, int Nk, int d,
                                int causal, int window, float sm_scale, attn_dtype_t dtype, void *workspace,
                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes attn_fwd_kv_int8 wants for these sizes on the current
+ * device; 0 when the shape takes no split-KV path.  No device work. */
+size_t attn_fwd_kv_int8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 
 /* Backward pass: the gradients of the forward definition for an upstream
  * gradient dO (the pages store the log-sum-exp "for the backward pass":

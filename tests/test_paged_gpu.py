@@ -88,16 +88,21 @@ def test_merge_paths(attn, oracle_mod, Hq, Hkv, Nq, max_len):
 
 
 def test_matches_flat_cache_bitwise(attn):
-    """With every request at the full length, the paged call computes the
-    same tiles as the flat call on the gathered cache: identical bits."""
-    shape = ai.PagedShape(4, 32, 8, 1, 8192, 128, 16, "bf16", True, 0, None, (8192,) * 4, 1, 0)
+    """With every request at the full length and the same chunk plan (32
+    requests of 2048 tokens: one chunk each, flat and paged alike), the
+    paged call computes the same tiles as the flat call on the gathered
+    cache: identical bits."""
+    B, L = 32, 2048
+    assert attn.attn_fwd_decode_plan(B, 32, 8, 1, L, 128, False, 152, 2) == \
+        attn.attn_fwd_decode_plan(B, 32, 8, 1, L, 128, True, 152, 2)
+    shape = ai.PagedShape(B, 32, 8, 1, L, 128, 16, "bf16", True, 0, None, (L,) * B, 1, 0)
     q, k, v, table, lens = ai.make_paged(shape, 104, 0)
     o, lse = run_paged(attn, shape, q, k, v, table, lens)
     idx = table.long()  # (B, pages)
-    kf = k[idx].permute(0, 2, 1, 3, 4).reshape(4, 8, 8192, 128)
-    vf = v[idx].permute(0, 2, 1, 3, 4).reshape(4, 8, 8192, 128)
-    flat = ai.AttnShape(4, 32, 8, 1, 8192, 128, "bf16", True)
-    nb = attn.attn_fwd_workspace_bytes(4, 32, 8, 1, 8192, 128)
+    kf = k[idx].permute(0, 2, 1, 3, 4).reshape(B, 8, L, 128)
+    vf = v[idx].permute(0, 2, 1, 3, 4).reshape(B, 8, L, 128)
+    flat = ai.AttnShape(B, 32, 8, 1, L, 128, "bf16", True)
+    nb = attn.attn_fwd_workspace_bytes(B, 32, 8, 1, L, 128)
     of, lf = pu.run_cuda(flat, q, kf, vf, workspace=torch.empty(nb, dtype=torch.uint8, device="cuda:0"))
     assert torch.equal(o.cpu(), of.cpu())
     assert torch.equal(lse.cpu(), lf.cpu())
@@ -193,15 +198,15 @@ def test_workload_full_size(attn, oracle_mod, idx):
 
 
 def test_paged_plan(attn):
-    """The paged plan caps the keys per chunk (lengths are known only on the
-    device): the ragged benchmark call keeps the fused merge, the group too
-    large for the split-KV kernel takes the prefill path, and a full-length call
-    that already splits finely plans like the flat call."""
+    """The paged plan keeps two CTAs per SM and caps the keys per chunk
+    (lengths are known only on the device): the ragged benchmark call keeps
+    the fused merge, the group too large for the split-KV kernel takes the
+    prefill path, and a full-length call plans more chunks than the flat
+    call (one long chunk per SM), so it needs more scratch."""
     assert attn.attn_fwd_paged_path(32, 32, 8, 1, 8192, 128) == attn.ATTN_PATH_SPLIT_KV_FUSED
     assert attn.attn_fwd_paged_path(1, 8, 1, 8, 256, 64) == attn.ATTN_PATH_PREFILL
     assert attn.attn_fwd_paged_path(4, 32, 8, 1, 8192, 128) == attn.attn_fwd_path(4, 32, 8, 1, 8192, 128, True)
-    assert attn.attn_fwd_paged_workspace_bytes(4, 32, 8, 1, 8192, 128) == \
+    assert attn.attn_fwd_paged_workspace_bytes(4, 32, 8, 1, 8192, 128) > \
         attn.attn_fwd_workspace_bytes(4, 32, 8, 1, 8192, 128)
-    # a long-context batch: more chunks than the flat plan, so more scratch
-    assert attn.attn_fwd_paged_workspace_bytes(32, 32, 8, 1, 8192, 128) > \
-        attn.attn_fwd_workspace_bytes(32, 32, 8, 1, 8192, 128)
+    assert attn.attn_fwd_paged_workspace_bytes(32, 32, 8, 1, 8192, 128) == \
+        attn.attn_fwd_workspace_bytes(32, 32, 8, 1, 8192, 128)  # 4 chunks of 2048 keys either way

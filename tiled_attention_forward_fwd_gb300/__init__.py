@@ -37,7 +37,7 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
             "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8", "attn_bwd", "attn_bwd_workspace_bytes",
-            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes", "attn_empty_launch"]
+            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes", "attn_empty_launch", "attn_fwd_kv_int8_workspace_bytes"]
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.attn_set_test_stall.restype = None
         L.attn_fwd_kv_int8.argtypes = [vp, vp, vp, cf, cf, vp, vp] + [ci] * 8 + [cf, ci, vp, sz, vp]
         L.attn_fwd_kv_int8.restype = ci
+        L.attn_fwd_kv_int8_workspace_bytes.argtypes = [ci] * 6
+        L.attn_fwd_kv_int8_workspace_bytes.restype = sz
         L.attn_bwd.argtypes = [vp] * 9 + [ci] * 8 + [cf, ci, vp, sz, vp]
         L.attn_bwd.restype = ci
         L.attn_bwd_workspace_bytes.argtypes = [ci] * 4
@@ -133,9 +135,10 @@ def attn_fwd_path(B, Hq, Hkv, Nq, Nk, d, with_workspace) -> int:
 
 def attn_fwd_decode_plan(B, Hq, Hkv, Nq, Nk, d, paged, sms, ctas_per_sm):
     """The split-KV plan without device work: dict(nchunks, chunk_keys,
-    fused, flag_off, bytes), or None when the shape takes no split-KV path."""
+    fused, flag_off, bytes), or None when the shape takes no split-KV path.
+    ``paged``: False / 0 flat cache, True / 1 paged cache, 2 int8 cache."""
     info = (ctypes.c_longlong * 5)()
-    if lib().attn_fwd_decode_plan(B, Hq, Hkv, Nq, Nk, d, 1 if paged else 0, sms, ctas_per_sm, info) != 0:
+    if lib().attn_fwd_decode_plan(B, Hq, Hkv, Nq, Nk, d, int(paged), sms, ctas_per_sm, info) != 0:
         return None
     return dict(zip(("nchunks", "chunk_keys", "fused", "flag_off", "bytes"), (int(x) for x in info)))
 
@@ -172,6 +175,10 @@ def attn_fwd_kv_int8(Q, K_codes, V_codes, k_scale, v_scale, O, LSE, B, Hq, Hkv, 
     return lib().attn_fwd_kv_int8(Q, K_codes, V_codes, float(k_scale), float(v_scale), O, LSE, B, Hq, Hkv, Nq, Nk, d,
                                   int(causal), int(window), float(sm_scale), int(dtype), workspace,
                                   int(workspace_bytes), stream)
+
+
+def attn_fwd_kv_int8_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
+    return int(lib().attn_fwd_kv_int8_workspace_bytes(B, Hq, Hkv, Nq, Nk, d))
 
 
 def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Nq, Nk, d, causal, window, sm_scale, dtype, workspace,
@@ -352,8 +359,8 @@ def flash_attn_kv_int8(q, k_codes, v_codes, k_scale: float, v_scale: float, caus
     """Decode over an INT8 K/V cache (see attn_fwd_kv_int8 in include/attn.h):
     K = k_scale * k_codes, V = v_scale * v_codes.  q: (B, Hq, Nq, d) fp16 or
     bf16; k_codes, v_codes: (B, Hkv, Nk, d) int8, on q's device.
-    ``workspace`` (a CUDA byte tensor of at least ``attn_fwd_workspace_bytes``
-    bytes) is allocated when not given.  Returns ``(O, LSE)``.  Runs on the
+    ``workspace`` (a CUDA byte tensor of at least
+    ``attn_fwd_kv_int8_workspace_bytes`` bytes) is allocated when not given.  Returns ``(O, LSE)``.  Runs on the
     current stream."""
     torch = _torch()
     if not (q.is_cuda and k_codes.is_cuda and v_codes.is_cuda):
@@ -373,7 +380,7 @@ def flash_attn_kv_int8(q, k_codes, v_codes, k_scale: float, v_scale: float, caus
     if return_lse and lse is None:
         lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
     if workspace is None:
-        need = attn_fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
+        need = attn_fwd_kv_int8_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     st = attn_fwd_kv_int8(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(), k_scale, v_scale, out.data_ptr(),
                           lse.data_ptr() if return_lse else None, B, Hq, Hkv, Nq, Nk, d, causal, window, scale,

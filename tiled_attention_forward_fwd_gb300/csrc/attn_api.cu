@@ -650,14 +650,27 @@ static int decode_ctas_per_sm(int d, int rb) {
 // most this many K/V tiles (chunks past a short request's end are empty and
 // end at once).
 constexpr int kPagedMaxChunkTiles = 32;
+constexpr int kDecCtaCostTiles = 6;  // fixed cost of a flat split-KV CTA, in K/V tiles
 
 // The split-KV path serves shapes whose GQA group holds at most 32 query rows
 // (decode: Nq = 1 with up to 32 query heads per K/V head).  The number of
-// chunks per group minimises (waves of CTAs) x (K/V tiles per CTA + a fixed
-// cost of about two tiles per CTA): usually one full wave of resident CTAs.
-// `ragged` (paged calls) also caps the tiles per chunk.
+// chunks per group minimises an estimate of the time:
+// - flat calls: (CTAs per SM) x (K/V tiles per CTA + 6).  The K/V stream of
+//   a CTA is bound by the copies it keeps in flight, and the SM's CTAs
+//   share its bandwidth, so what counts is the tiles an SM streams plus a
+//   fixed cost per CTA (start, first-tile latency, partial write, merge) of
+//   about six tiles: one long chunk per SM beats two CTAs of half the length
+//   (on GB300, 4 chunks x 32 groups: 33.0 us against 35.1 us for 9 chunks
+//   at two CTAs per SM, for 8192 keys at d = 128);
+// - paged calls: (waves of resident CTAs) x (tiles per CTA + 2), then at
+//   most 32 tiles per chunk.  Their producer issues one copy per page, so
+//   two resident CTAs per SM (two producers) pay;
+// - int8 K/V: the same waves model without the cap.  Its consumers widen
+//   every tile before the MMAs, so two CTAs per SM (twice the warps) pay
+//   (38.1 us against 51.3 us with the flat model's 4 chunks at Hkv = 8).
 // The plan for a device of `sms` SMs with `per_sm` resident split CTAs each.
-static DecPlan decode_plan_for(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool ragged, int sms, int per_sm) {
+enum DecPlanMode : int { kPlanFlat = 0, kPlanPaged = 1, kPlanQuant = 2 };
+static DecPlan decode_plan_for(int B, int Hq, int Hkv, int Nq, int Nk, int d, int mode, int sms, int per_sm) {
   DecPlan pl;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return pl;
   const long long R = static_cast<long long>(Hq / Hkv) * Nq;
@@ -670,14 +683,15 @@ static DecPlan decode_plan_for(int B, int Hq, int Hkv, int Nq, int Nk, int d, bo
   const long long max_n = std::min<long long>(std::min<long long>(tiles, kDecMaxChunks), 4 * slots / units + 1);
   long long best_n = 1, best_cost = -1;
   for (long long n = 1; n <= max_n; ++n) {
-    const long long waves = (units * n + slots - 1) / slots;
-    const long long cost = waves * ((tiles + n - 1) / n + 2);
+    const long long per_tile = (tiles + n - 1) / n;
+    const long long cost = mode != kPlanFlat ? ((units * n + slots - 1) / slots) * (per_tile + 2)
+                                             : ((units * n + sms - 1) / sms) * (per_tile + kDecCtaCostTiles);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_n = n;
     }
   }
-  if (ragged) {
+  if (mode == kPlanPaged) {
     const long long cap_n = (tiles + kPagedMaxChunkTiles - 1) / kPagedMaxChunkTiles;
     best_n = std::max(best_n, std::min<long long>(cap_n, kDecMaxChunks));
   }
@@ -695,11 +709,11 @@ static DecPlan decode_plan_for(int B, int Hq, int Hkv, int Nq, int Nk, int d, bo
   return pl;
 }
 
-static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, bool ragged = false) {
+static DecPlan decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int mode = kPlanFlat) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128)) return {};
   const long long R = static_cast<long long>(Hq / Hkv) * Nq;
   if (R > kDecMaxRows) return {};
-  return decode_plan_for(B, Hq, Hkv, Nq, Nk, d, ragged, device_sm_count(), decode_ctas_per_sm(d, R <= 16 ? 1 : 2));
+  return decode_plan_for(B, Hq, Hkv, Nq, Nk, d, mode, device_sm_count(), decode_ctas_per_sm(d, R <= 16 ? 1 : 2));
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
@@ -974,7 +988,7 @@ attn_status_t attn_fwd_paged(const void *Q, const void *K_pages, const void *V_p
   if (static_cast<long long>(num_pages) * Hkv >= 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
   const PagedKV pg{block_table, seq_lens, page_size, num_pages, max_pages_per_seq};
-  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, kPlanPaged);
   if (pl.bytes == 0) {
     // groups of more than 32 query rows: the tiled prefill kernel on the pages
     if (static_cast<long long>(B) * Hq * ((Nq + kBM - 1) / kBM) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
@@ -994,11 +1008,15 @@ attn_status_t attn_fwd_kv_int8(const void *Q, const void *K_codes, const void *V
   if (!std::isfinite(k_scale) || !(k_scale > 0.f) || !std::isfinite(v_scale) || !(v_scale > 0.f))
     return ATTN_ERR_INVALID_ARG;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
-  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, Nk, d);
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, Nk, d, kPlanQuant);
   if (pl.bytes == 0) return ATTN_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   const QuantKV qk{k_scale, v_scale};
   return dispatch_decode(Q, K_codes, V_codes, O, LSE, s, pl, static_cast<float *>(workspace), stream, nullptr, &qk);
+}
+
+size_t attn_fwd_kv_int8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  return decode_plan(B, Hq, Hkv, Nq, Nk, d, kPlanQuant).bytes;
 }
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq, int d) {
@@ -1060,14 +1078,14 @@ attn_status_t attn_fwd_mla(const void *Q_lat, const void *C_lat, void *O_lat, fl
 
 int attn_fwd_paged_path(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || max_seq_len <= 0 || (d != 64 && d != 128) || Hq % Hkv) return -1;
-  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true);
+  const DecPlan pl = decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, kPlanPaged);
   if (pl.bytes == 0) return ATTN_PATH_PREFILL;  // larger query groups: the tiled prefill kernel
   return pl.fused ? ATTN_PATH_SPLIT_KV_FUSED : ATTN_PATH_SPLIT_KV;
 }
 
 size_t attn_fwd_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_seq_len, int d) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || max_seq_len <= 0 || (d != 64 && d != 128) || Hq % Hkv) return 0;
-  return decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, true).bytes;
+  return decode_plan(B, Hq, Hkv, Nq, max_seq_len, d, kPlanPaged).bytes;
 }
 
 int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_workspace) {
@@ -1083,7 +1101,8 @@ int attn_fwd_path(int B, int Hq, int Hkv, int Nq, int Nk, int d, int with_worksp
 int attn_fwd_decode_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int paged, int sms, int ctas_per_sm,
                          long long *info) {
   if (info == nullptr) return -1;
-  const DecPlan pl = decode_plan_for(B, Hq, Hkv, Nq, Nk, d, paged != 0, sms, ctas_per_sm);
+  if (paged < 0 || paged > 2) return -1;
+  const DecPlan pl = decode_plan_for(B, Hq, Hkv, Nq, Nk, d, paged, sms, ctas_per_sm);
   if (pl.bytes == 0) return -1;
   info[0] = pl.nchunks;
   info[1] = pl.chunk_keys;
