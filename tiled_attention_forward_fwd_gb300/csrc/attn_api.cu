@@ -945,6 +945,173 @@ static attn_status_t run(const void *Q, const void *K, const void *V, void *O, f
   return dispatch_prefill(Q, K, V, O, LSE, s, ws, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- host-buffer calls, pipelined
+// A large call on host buffers is cut into pieces: contiguous ranges of
+// (request, K/V head) slabs, each a contiguous byte range of Q, K, V, O and
+// LSE and a call of its own.  A piece's inputs are copied in on one internal
+// stream, its kernel runs on the caller's stream once they have arrived, and
+// its outputs are copied out on a second internal stream: the copies of one
+// piece overlap the compute of its neighbours (copy-in, compute and copy-out
+// each go in piece order).  Pieces are used only when each is computed with
+// the schedule and item shape of the whole call (the plain prefill, the same
+// pairing of query tiles), so the results are the same bits.
+constexpr int kHostMaxPieces = 16;
+constexpr int kHostTargetPieces = 8;
+constexpr size_t kHostPipeMinBytes = size_t(64) << 20;  // Q + K + V below this: copy, compute, copy
+
+struct HostPiece {
+  int b0, nb;  // requests [b0, b0 + nb)
+  int h0, nh;  // K/V heads [h0, h0 + nh) of each (all of them when nb > 1)
+};
+
+// Per device: two copy streams and the events that chain the pieces.
+struct HostPipe {
+  std::mutex mu;  // one pipelined enqueue at a time per device (the events are shared)
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+  cudaEvent_t ev_in[kHostMaxPieces] = {}, ev_comp[kHostMaxPieces] = {};
+};
+
+static HostPipe &host_pipe(int dev) {
+  static HostPipe pipes[64];
+  return pipes[dev];
+}
+
+// Creates the streams and events on first use (the caller holds hp.mu and has
+// the device current).  A failure is not cached: everything made so far is
+// released, the error cleared, and the next call tries again.
+static bool host_pipe_init(HostPipe &hp) {
+  if (hp.ready) return true;
+  bool ok = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.ev_end, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kHostMaxPieces; ++i)
+    ok = cudaEventCreateWithFlags(&hp.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
+  if (ok) {
+    hp.ready = true;
+    return true;
+  }
+  for (int i = 0; i < kHostMaxPieces; ++i) {
+    if (hp.ev_in[i]) cudaEventDestroy(hp.ev_in[i]);
+    if (hp.ev_comp[i]) cudaEventDestroy(hp.ev_comp[i]);
+    hp.ev_in[i] = hp.ev_comp[i] = nullptr;
+  }
+  if (hp.ev_start) cudaEventDestroy(hp.ev_start);
+  if (hp.ev_end) cudaEventDestroy(hp.ev_end);
+  if (hp.s_in) cudaStreamDestroy(hp.s_in);
+  if (hp.s_out) cudaStreamDestroy(hp.s_out);
+  hp.ev_start = hp.ev_end = nullptr;
+  hp.s_in = hp.s_out = nullptr;
+  cudaGetLastError();
+  return false;
+}
+
+// The pieces of a host-buffer call, or 0 when it is not cut: small calls,
+// one slab, and shapes whose pieces would be scheduled differently from the
+// whole call (a split path, few query tiles, another pairing).
+static int host_pieces(const Shape &s, HostPiece *out) {
+  if (s.d != 64 && s.d != 128) return 0;
+  const size_t q = static_cast<size_t>(s.B) * s.Hq * s.Nq * s.d * 2;
+  const size_t kv = static_cast<size_t>(s.B) * s.Hkv * s.Nk * s.d * 2;
+  if (q + 2 * kv < kHostPipeMinBytes || static_cast<long long>(s.B) * s.Hkv < 2) return 0;
+  if (short_path(s) || workspace_bytes(s.B, s.Hq, s.Hkv, s.Nq, s.Nk, s.d) > 0) return 0;  // decode or split
+  int n = 0;
+  if (s.B >= kHostTargetPieces) {
+    for (int i = 0; i < kHostTargetPieces; ++i) {
+      const int b0 = static_cast<int>(static_cast<long long>(i) * s.B / kHostTargetPieces);
+      const int b1 = static_cast<int>(static_cast<long long>(i + 1) * s.B / kHostTargetPieces);
+      out[n++] = HostPiece{b0, b1 - b0, 0, s.Hkv};
+    }
+  } else {
+    const int per_b = std::min(s.Hkv, (kHostTargetPieces + s.B - 1) / s.B);
+    if (static_cast<long long>(s.B) * per_b > kHostMaxPieces) return 0;
+    for (int b = 0; b < s.B; ++b)
+      for (int j = 0; j < per_b; ++j) {
+        const int h0 = j * s.Hkv / per_b, h1 = (j + 1) * s.Hkv / per_b;
+        out[n++] = HostPiece{b, 1, h0, h1 - h0};
+      }
+  }
+  if (n < 2) return 0;
+  // every piece on the plain schedule with the whole call's pairing
+  const int sms = device_sm_count();
+  FwdParams pw, pp;
+  int sw = 0, gw = 0, sp = 0, gp = 0;
+  if (!prefill_schedule(s, false, sms, pw, sw, gw) || sw != kSchedPlain) return 0;
+  const int g = s.Hq / s.Hkv;
+  for (int i = 0; i < n; ++i) {
+    const Shape ps{out[i].nb, out[i].nh * g, out[i].nh, s.Nq, s.Nk, s.d, s.causal, s.window, s.sm_scale, s.dtype};
+    if (!prefill_schedule(ps, false, sms, pp, sp, gp) || sp != kSchedPlain || pp.pair_mode != pw.pair_mode) return 0;
+  }
+  return n;
+}
+
+// Enqueues the pieces of a host-buffer call (device buffers dQ..dL hold the
+// whole call; host pointers are its host arrays).  `stream` is forked to the
+// two copy streams at the start and joined at the end, so the call as a
+// whole still follows and precedes the work around it on `stream` (also
+// under CUDA-graph capture).  On a CUDA error the streams are still joined.
+static attn_status_t host_pipelined(const uint8_t *Qh, const uint8_t *Kh, const uint8_t *Vh, uint8_t *Oh,
+                                    float *Lh, const Shape &s, const HostPiece *pc, int np, uint8_t *dQ,
+                                    uint8_t *dK, uint8_t *dV, uint8_t *dO, float *dL, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  HostPipe &hp = host_pipe(dev);
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if (!host_pipe_init(hp)) return ATTN_ERR_CUDA;
+  const int g = s.Hq / s.Hkv;
+  const size_t qh_bytes = static_cast<size_t>(s.Nq) * s.d * 2;   // one query head
+  const size_t kvh_bytes = static_cast<size_t>(s.Nk) * s.d * 2;  // one K/V head
+  bool ok = cudaEventRecord(hp.ev_start, stream) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.s_in, hp.ev_start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.s_out, hp.ev_start, 0) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  attn_status_t st = ATTN_OK;
+  for (int i = 0; i < np && ok && st == ATTN_OK; ++i) {
+    const HostPiece &p = pc[i];
+    const size_t q0 = static_cast<size_t>(p.b0) * s.Hq + static_cast<size_t>(p.h0) * g;  // first query head
+    const size_t nq = static_cast<size_t>(p.nb) * p.nh * g;                                // query heads
+    const size_t k0 = static_cast<size_t>(p.b0) * s.Hkv + p.h0;                          // first K/V head
+    const size_t nkv = static_cast<size_t>(p.nb) * p.nh;
+    ok = cudaMemcpyAsync(dQ + q0 * qh_bytes, Qh + q0 * qh_bytes, nq * qh_bytes, cudaMemcpyHostToDevice,
+                         hp.s_in) == cudaSuccess &&
+         cudaMemcpyAsync(dK + k0 * kvh_bytes, Kh + k0 * kvh_bytes, nkv * kvh_bytes, cudaMemcpyHostToDevice,
+                         hp.s_in) == cudaSuccess &&
+         cudaMemcpyAsync(dV + k0 * kvh_bytes, Vh + k0 * kvh_bytes, nkv * kvh_bytes, cudaMemcpyHostToDevice,
+                         hp.s_in) == cudaSuccess &&
+         cudaEventRecord(hp.ev_in[i], hp.s_in) == cudaSuccess &&
+         cudaStreamWaitEvent(stream, hp.ev_in[i], 0) == cudaSuccess;
+    if (!ok) break;
+    const Shape ps{p.nb, p.nh * g, p.nh, s.Nq, s.Nk, s.d, s.causal, s.window, s.sm_scale, s.dtype};
+    float *dLp = dL ? dL + q0 * s.Nq : nullptr;
+    st = run(dQ + q0 * qh_bytes, dK + k0 * kvh_bytes, dV + k0 * kvh_bytes, dO + q0 * qh_bytes, dLp, ps, nullptr, 0,
+             stream);
+    if (st != ATTN_OK) break;
+    ok = cudaEventRecord(hp.ev_comp[i], stream) == cudaSuccess &&
+         cudaStreamWaitEvent(hp.s_out, hp.ev_comp[i], 0) == cudaSuccess &&
+         cudaMemcpyAsync(Oh + q0 * qh_bytes, dO + q0 * qh_bytes, nq * qh_bytes, cudaMemcpyDeviceToHost,
+                         hp.s_out) == cudaSuccess &&
+         (Lh == nullptr || cudaMemcpyAsync(Lh + q0 * s.Nq, dLp, nq * s.Nq * sizeof(float), cudaMemcpyDeviceToHost,
+                                           hp.s_out) == cudaSuccess);
+  }
+  // join both copy streams back into `stream`, also after an error
+  const bool joined = cudaEventRecord(hp.ev_end, hp.s_out) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, hp.ev_end, 0) == cudaSuccess &&
+                      cudaEventRecord(hp.ev_start, hp.s_in) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, hp.ev_start, 0) == cudaSuccess;
+  if (st != ATTN_OK) return st;
+  if (!ok || !joined) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -1193,6 +1360,14 @@ attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *
   void *dW = ws_bytes ? base + 2 * round_up256(q) + 2 * round_up256(kv) + round_up256(lse_bytes) : nullptr;
   attn_status_t st = validate(dQ, dK, dV, dO, dL, s);
   if (st != ATTN_OK) return st;
+  if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  HostPiece pieces[kHostMaxPieces];
+  const int np = host_pieces(s, pieces);
+  if (np > 0)
+    return host_pipelined(static_cast<const uint8_t *>(Q_host), static_cast<const uint8_t *>(K_host),
+                          static_cast<const uint8_t *>(V_host), static_cast<uint8_t *>(O_host), LSE_host, s, pieces, np,
+                          static_cast<uint8_t *>(dQ), static_cast<uint8_t *>(dK), static_cast<uint8_t *>(dV),
+                          static_cast<uint8_t *>(dO), dL, stream);
   if (cudaMemcpyAsync(dQ, Q_host, q, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, stream) != cudaSuccess)
