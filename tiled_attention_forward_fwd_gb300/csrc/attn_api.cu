@@ -68,6 +68,22 @@ static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view (d, rows, slabs) of a dense (slabs, rows, d) fp32 tensor, box 32 x
+// 128 x 1 with the 128-byte swizzle (the backward's dQ accumulator, written
+// by TMA reduce-adds).
+static bool make_map_f32(CUtensorMap *m, void *ptr, int d, int rows, long long slabs) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slabs)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(d) * 4 * rows};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D view (d, rows, slabs) of a dense (slabs, rows, d) int8 tensor, box d x
 // 64 x 1 without swizzle (the decode kernel widens rows itself).
 static bool make_map_s8(CUtensorMap *m, const void *ptr, int d, int rows, long long slabs) {
@@ -388,6 +404,7 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   const long long rows = zq * s.Nq;
   uint8_t *base = static_cast<uint8_t *>(ws);
   p.dq_acc = reinterpret_cast<float *>(base);
+  if (!make_map_f32(&p.tmDQ, p.dq_acc, D, s.Nq, zq)) return ATTN_ERR_CUDA;
   p.delta = reinterpret_cast<const float *>(base + round_up256(static_cast<size_t>(rows) * D * 4));
   p.lse = LSE;
   p.dK = dK;

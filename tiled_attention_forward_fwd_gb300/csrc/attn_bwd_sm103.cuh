@@ -28,7 +28,10 @@
 //      MN-major), accumulated in TMEM over the CTA's steps; dQ_part = dS K_j
 //      (A K-major, B = K_j MN-major) into TMEM.
 //   5. Thread r adds its dQ_part row to an fp32 accumulator in global memory
-//      (vector reductions; several CTAs add to one row).
+//      (vector reductions; several CTAs add to one row), while the next
+//      step's Q and dO load (their buffers are free once step 4's MMAs,
+//      the last to read them, have completed).
+// Each group of MMAs is issued in bursts of four from one asm block.
 // At the end the CTA writes dK (times sm_scale) and dV for its 128 keys.  A
 // pre-pass computes D and zeroes the dQ accumulator; a post-pass writes dQ.
 #pragma once
@@ -45,6 +48,7 @@ struct BwdParams {
   CUtensorMap tmDO;  // (d, Nq, B*Hq)
   CUtensorMap tmK;   // (d, Nk, B*Hkv)
   CUtensorMap tmV;   // (d, Nk, B*Hkv)
+  CUtensorMap tmDQ;  // the fp32 dQ accumulator (d, Nq, B*Hq), box 32 x 128 x 1, 128B swizzle
   const float *lse;    // (B*Hq*Nq) natural-log LSE of the forward
   const float *delta;  // (B*Hq*Nq) rowsum(dO o O)
   float *dq_acc;       // (B*Hq*Nq*d) fp32, zeroed by the pre-pass
@@ -75,30 +79,45 @@ struct BwdCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// 16x(MN = 128) x K tile product with both operands MN-major (A = P or dS
-// stored [K row][M], B = dO or Q stored [K row][N]): 8 K-slices of 16 rows,
-// each 2048 bytes (128 descriptor units) further in both.
+// Four MMAs issued back to back in one asm block (a tcgen05.mma issued on
+// its own costs about twice the cycles of one in such a burst): D (+)=
+// A_k B_k for the four (a_k, b_k) descriptor pairs; the first accumulates
+// iff `accumulate` != 0, the others always.
+__device__ __forceinline__ void umma_ss_burst4(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
+                                               uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, p1;\n\t"
+      "setp.ne.b32 pf, %9, 0;\n\tsetp.eq.b32 p1, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, p1;\n\t}\n" ::"r"(d),
+      "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(accumulate), "r"(idesc)
+      : "memory");
+}
+
+// (MN = 128) x N tile product over K = 128 with both operands MN-major (A =
+// P or dS stored [K row][M], B = dO or Q stored [K row][N]): 8 K-slices of
+// 16 rows, each 2048 bytes (128 descriptor units) further in both.
 __device__ __forceinline__ void umma_mn_mn_x8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) umma_ss(d, a + 128ull * k, b + 128ull * k, idesc, (k > 0) ? 1u : acc);
+  umma_ss_burst4(d, a, a + 128, a + 256, a + 384, b, b + 128, b + 256, b + 384, idesc, acc);
+  umma_ss_burst4(d, a + 512, a + 640, a + 768, a + 896, b + 512, b + 640, b + 768, b + 896, idesc, 1u);
 }
 // K = 128 with A K-major (dS stored [M row][K], two 64-column boxes: 32
 // bytes per slice within a box, 16 KB to the next box) and B MN-major (K_j
 // stored [K row][N]: 2048 bytes per slice).
 __device__ __forceinline__ void umma_k_mn_x8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    umma_ss(d, a + ((k >= 4) ? 1024ull : 0ull) + 2ull * (k & 3), b + 128ull * k, idesc, (k > 0) ? 1u : 0u);
+  umma_ss_burst4(d, a, a + 2, a + 4, a + 6, b, b + 128, b + 256, b + 384, idesc, 0u);
+  umma_ss_burst4(d, a + 1024, a + 1026, a + 1028, a + 1030, b + 512, b + 640, b + 768, b + 896, idesc, 1u);
 }
 // S = A B^T with both K-major (Q or dO against K or V): D / 16 K-slices, 32
 // bytes per slice within a 64-column box, 16 KB to the next box.
 template <int D>
 __device__ __forceinline__ void umma_k_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-#pragma unroll
-  for (int k = 0; k < D / 16; ++k) {
-    const uint64_t o = ((k >= 4) ? 1024ull : 0ull) + 2ull * (k & 3);
-    umma_ss(d, a + o, b + o, idesc, (k > 0) ? 1u : 0u);
-  }
+  umma_ss_burst4(d, a, a + 2, a + 4, a + 6, b, b + 2, b + 4, b + 6, idesc, 0u);
+  if constexpr (D == 128)
+    umma_ss_burst4(d, a + 1024, a + 1026, a + 1028, a + 1030, b + 1024, b + 1026, b + 1028, b + 1030, idesc, 1u);
 }
 
 // Bounded wait that ignores the abort flag: used only to drain our own
@@ -107,11 +126,6 @@ __device__ __forceinline__ void mbar_drain_plain(uint32_t bar, uint32_t parity) 
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
     if (clock64() - t0 > 3000000000ll) break;
-}
-
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 template <int D, bool BF16>
@@ -154,6 +168,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     if (elect_one()) {
       tma_prefetch_desc(&p.tmQ);
       tma_prefetch_desc(&p.tmDO);
+      tma_prefetch_desc(&p.tmDQ);
       mbar_arrive_expect_tx(bKV, 2 * C::kTileBytes);
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -182,23 +197,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
   constexpr uint32_t kIdT = idesc_f16(128, D, BF16, true, true);   // P^T dO, dS^T Q
   constexpr uint32_t kIdQ = idesc_f16(128, D, BF16, false, true);  // dS K
   const float log2e = 1.4426950408889634074f;
-  int step = 0;
+  // The steps: every query head of the group, then every live query tile.
+  const int nq_per = i_hi > i_lo ? i_hi - i_lo : 0;
+  const int nsteps = p.group * nq_per;
   int issued_q = 0;  // Q / dO loads issued (drained on the way out)
-  for (int hh = 0; hh < p.group; ++hh) {
+  // Q_i and dO_i of step st into their (single) buffers, by warp 0
+  auto issue_load = [&](int st) {
+    if (warp != 0) return;
+    const int hh = st / nq_per, qt = i_lo + st - hh * nq_per;
     const int zq = b * p.Hq + kvh * p.group + hh;
-    for (int qt = i_lo; qt < i_hi; ++qt, ++step) {
-      if (warp == 0) {
-        if (ok && elect_one()) {
-          mbar_arrive_expect_tx(bQ, 2 * C::kTileBytes);
+    if (ok && elect_one()) {
+      mbar_arrive_expect_tx(bQ, 2 * C::kTileBytes);
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {
-            tma_load_3d(sQ + cc * C::kBoxBytes, &p.tmQ, bQ, cc * 64, qt * 128, zq);
-            tma_load_3d(sDO + cc * C::kBoxBytes, &p.tmDO, bQ, cc * 64, qt * 128, zq);
-          }
-        }
-        __syncwarp();
-        if (ok) issued_q = step + 1;
+      for (int cc = 0; cc < D / 64; ++cc) {
+        tma_load_3d(sQ + cc * C::kBoxBytes, &p.tmQ, bQ, cc * 64, qt * 128, zq);
+        tma_load_3d(sDO + cc * C::kBoxBytes, &p.tmDO, bQ, cc * 64, qt * 128, zq);
       }
+    }
+    __syncwarp();
+    if (ok) issued_q = st + 1;
+  };
+  if (nsteps > 0) issue_load(0);
+  int step = 0;
+  for (; step < nsteps; ++step) {
+    {
+      const int hh = step / nq_per, qt = i_lo + step - hh * nq_per;
+      const int zq = b * p.Hq + kvh * p.group + hh;
       const int qrow = qt * 128 + row;
       const bool live_row = qrow < p.Nq;
       const size_t grow = static_cast<size_t>(zq) * p.Nq + (live_row ? qrow : 0);
@@ -217,6 +241,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
       }
       ok = ok && mbar_wait_warp(bS, step & 1, wc, kErrBwdWait);
       tc_fence_after();
+      if (step > 0) {  // the previous step's dQ reduce has read its staging tile (the P and dS buffers)
+        if (threadIdx.x == 0) tma_store_wait_read0();
+        __syncthreads();
+      }
       // ---- P and dS of this row -> shared memory, 16-bit, swizzled [row][key]
       const int pos = qrow + off;
       const int key0 = kt * 128;
@@ -270,21 +298,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
       }
       ok = ok && mbar_wait_warp(bD, step & 1, wc, kErrBwdWait);
       tc_fence_after();
-      // ---- this row's dQ_part into the fp32 accumulator
-      float *dst = p.dq_acc + grow * D;
+      // every MMA that reads Q_i and dO_i has completed: the next step's
+      // tiles load while this step's dQ_part goes out
+      if (step + 1 < nsteps) issue_load(step + 1);
+      // ---- dQ_part of the tile into the fp32 accumulator: each row from TMEM
+      // into an fp32 staging tile in the P and dS buffers (free: the MMAs
+      // that read them have completed), D / 32 boxes of 128 rows x 32
+      // columns in the 128-byte swizzle (16-byte chunk q of row r at q ^ (r
+      // % 8): no bank conflicts), then one TMA reduce-add per box.  Rows past
+      // Nq are clipped by the tensor map.
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + cc * 32, r);
-        if (ok && live_row) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            red_add_v4(dst + cc * 32 + 4 * q, __uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t chunk = static_cast<uint32_t>(q) ^ static_cast<uint32_t>(row & 7);
+          st_shared_v4(sP + cc * 16384 + row * 128 + chunk * 16, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
         }
       }
+      fence_proxy_async_smem();  // the staged tile is visible to the TMA
       tc_fence_before();
-      __syncthreads();  // TMEM [0, 128) and the Q, dO, P, dS tiles are free for the next step
+      __syncthreads();  // the tile is staged; TMEM [0, 128) is free for the next step
+      if (threadIdx.x == 0 && ok) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_3d(&p.tmDQ, sP + cc * 16384, cc * 32, qt * 128, zq);
+        tma_store_commit();
+      }
     }
   }
   // ---- dK (times sm_scale) and dV of this key tile; zero where no query reached it
@@ -321,7 +361,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
       }
     }
   }
-  // Never leave with a copy or an MMA of ours in flight.
+  // Never leave with a copy or an MMA of ours in flight (the dQ reduces
+  // complete before the CTA's shared memory goes).
+  if (threadIdx.x == 0) tma_store_wait0();
   if (warp == 0) {
     if (elect_one()) {
       umma_commit(bDrain);
