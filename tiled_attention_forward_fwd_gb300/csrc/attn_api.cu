@@ -435,7 +435,7 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
                  dO, delta, p.dq_acc, rows) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const dim3 grid(static_cast<unsigned>((s.Nk + 127) / 128), static_cast<unsigned>(zk));
-  if (launch_pdl(attn_bwd_kernel<D, BF16>, grid, dim3(kBwdThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
+  if (launch_pdl(attn_bwd_kernel<D, BF16>, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const long long n4 = rows * D / 4;
   const int sms = std::max(1, device_sm_count());

@@ -13,24 +13,26 @@
 // with GQA heads summed into their K/V head.  The score matrix never reaches
 // device memory, as in the forward.
 //
-// GB300 mapping (a first, synchronous design: each step's MMAs and its
-// elementwise work alternate).  Grid (key tiles of 128 keys, B * Hkv); 128
-// threads, thread r owning TMEM lane r.  A CTA holds K_j and V_j in shared
+// GB300 mapping (a synchronous design: each step's MMAs and its elementwise
+// work alternate).  Grid (key tiles of 128 keys, B * Hkv); one thread per
+// TMEM lane r (query row, later key row) at d = 128, two at d = 64 (each
+// taking half of the row's columns in the elementwise passes).  A CTA holds K_j and V_j in shared
 // memory and walks every query head of the GQA group and every query tile
 // that has a live key in the tile:
 //   1. TMA Q_i and dO_i (128-row boxes, 128B swizzle).
 //   2. tcgen05: S = Q_i K_j^T and dP = dO_i V_j^T into TMEM (fp32).
-//   3. Thread r (query row r): P and dS of its row, rounded to the input
-//      dtype, into shared memory in the 128B-swizzled layout of a [row][key]
-//      tile (two 64-column boxes).
+//   3. The threads of lane r (query row r): P and dS of the row, rounded to
+//      the input dtype, into shared memory in the 128B-swizzled layout of a
+//      [row][key] tile (two 64-column boxes).
 //   4. tcgen05: dV += P^T dO_i and dK += dS^T Q_i (A = P / dS read
 //      MN-major, i.e. transposed, from the same tiles; B = dO_i / Q_i
 //      MN-major), accumulated in TMEM over the CTA's steps; dQ_part = dS K_j
 //      (A K-major, B = K_j MN-major) into TMEM.
-//   5. Thread r adds its dQ_part row to an fp32 accumulator in global memory
-//      (vector reductions; several CTAs add to one row), while the next
-//      step's Q and dO load (their buffers are free once step 4's MMAs,
-//      the last to read them, have completed).
+//   5. The tile's dQ_part goes from TMEM into an fp32 tile in the (now free)
+//      P and dS buffers, and TMA reduce-adds it into an fp32 accumulator in
+//      global memory (several CTAs add to one row), while the next step's Q
+//      and dO load (their buffers are free once step 4's MMAs, the last to
+//      read them, have completed).
 // Each group of MMAs is issued in bursts of four from one asm block.
 // At the end the CTA writes dK (times sm_scale) and dV for its 128 keys.  A
 // pre-pass computes D and zeroes the dQ accumulator; a post-pass writes dQ.
@@ -40,7 +42,6 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 128;
 enum BwdError : int { kErrBwdWait = 0x301 };
 
 struct BwdParams {
@@ -64,6 +65,11 @@ struct BwdParams {
 
 template <int D>
 struct BwdCfg {
+  // threads: one per TMEM lane at d = 128; two at d = 64, each taking half
+  // of a row's columns in the elementwise passes (measured: 415 -> 377 us on
+  // a d = 64 layer; 7.96 -> 8.22 ms at d = 128, so one there)
+  static constexpr int kThreads = D == 64 ? 256 : 128;
+  static constexpr int kPerLane = kThreads / 128;
   static constexpr int kBoxBytes = 128 * 128;   // 128 rows x 64 columns x 2 bytes
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kOffK = 0;
@@ -129,7 +135,7 @@ __device__ __forceinline__ void mbar_drain_plain(uint32_t bar, uint32_t parity) 
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,7 +147,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
   const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
   const uint32_t sP = smem_u32(smem + C::kOffP), sDS = smem_u32(smem + C::kOffDS);
   const int warp = threadIdx.x >> 5;
-  const int row = threadIdx.x;  // TMEM lane: a query row of the tile, later a key row
+  const int row = threadIdx.x & 127;  // TMEM lane: a query row of the tile, later a key row
+  const int half = threadIdx.x >> 7;   // which part of the row's columns this thread takes
   const int kt = blockIdx.x;
   const int bk = blockIdx.y;  // b * Hkv + kvh
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
   tc_fence_after();
   pdl_wait();  // D and the zeroed dQ accumulator come from the pre-pass
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;  // warp w reads lanes 32 (w % 4) ..
 
   if (warp == 0) {
     if (elect_one()) {
@@ -252,7 +259,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
       const int hi = live_row ? min(p.Nk, p.causal ? pos + 1 : p.Nk) - key0 : 0;
       const int lo = (p.causal && p.window > 0) ? pos - p.window + 1 - key0 : 0;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int c2 = 0; c2 < 4 / C::kPerLane; ++c2) {
+        const int cc = half * (4 / C::kPerLane) + c2;  // 32-column chunk of the 128 keys
         uint32_t sr[32], dpr[32];
         tmem_ld32(tmem + lane_off + cc * 32, sr);
         tmem_ld32(tmem + lane_off + C::kColDP + cc * 32, dpr);
@@ -308,7 +316,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
       // % 8): no bank conflicts), then one TMA reduce-add per box.  Rows past
       // Nq are clipped by the tensor map.
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int c2 = 0; c2 < D / 32 / C::kPerLane; ++c2) {
+        const int cc = half * (D / 32 / C::kPerLane) + c2;  // this thread's 32-column boxes
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + cc * 32, r);
 #pragma unroll
@@ -333,7 +342,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
   uint16_t *dk_out = reinterpret_cast<uint16_t *>(p.dK) + (static_cast<size_t>(bk) * p.Nk + (live_key ? key : 0)) * D;
   uint16_t *dv_out = reinterpret_cast<uint16_t *>(p.dV) + (static_cast<size_t>(bk) * p.Nk + (live_key ? key : 0)) * D;
 #pragma unroll
-  for (int cc = 0; cc < D / 32; ++cc) {
+  for (int c2 = 0; c2 < D / 32 / C::kPerLane; ++c2) {
+    const int cc = half * (D / 32 / C::kPerLane) + c2;
     uint32_t rk[32], rv[32];
     tmem_ld32(tmem + lane_off + C::kColDK + cc * 32, rk);
     tmem_ld32(tmem + lane_off + C::kColDV + cc * 32, rv);
