@@ -132,3 +132,25 @@ def test_errors(attn):
         attn.flash_attn_backward(q, q, q, q, lse, q, workspace=torch.empty(16, dtype=torch.uint8, device=dev))
     assert e.value.status == attn.ATTN_ERR_INVALID_ARG
     assert attn.device_status() == attn.ATTN_OK
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_wait_limit_then_recovery(attn, oracle_mod, d):
+    """Every wait of the backward is bounded: with a 1 ns limit (a wait that
+    polls more than once gives up) the call comes back with ATTN_OK or
+    ATTN_ERR_TIMEOUT, and with the default limit the next call on the same
+    buffers matches the oracle."""
+    s = ai.AttnShape(1, 4, 2, 300, 300, d, "bf16", True)
+    q, k, v = ai.make_qkv(s, config_id=190)
+    do = ai.normal_tensor(ai.seed_for(190, 0, "G"), tuple(q.shape), s.dtype)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = attn.flash_attn_forward(qd, kd, vd, causal=True)
+    try:
+        attn.attn_set_wait_timeout_ns(1)
+        for _ in range(3):
+            attn.flash_attn_backward(qd, kd, vd, o, lse, dod, causal=True)
+            st = attn.device_status()
+            assert st in (attn.ATTN_OK, attn.ATTN_ERR_TIMEOUT), attn.attn_status_string(st)
+    finally:
+        attn.attn_set_wait_timeout_ns(0)
+    check(attn, oracle_mod, s, 190)
