@@ -338,11 +338,13 @@ size_t attn_fwd_mla_workspace_bytes(int B, int n_h, int Nq, int Nk, int d_c);
  * inputs are copied in on an internal stream, its kernel runs on `stream`
  * after them, and its outputs are copied out on a second internal stream.
  * `stream` is forked to the internal streams at the start of the call and
- * joined at its end (also under CUDA-graph capture), and a piece is
- * computed with the same schedule as the whole call, so the results are
- * the same bits as without pieces.  The internal streams and events are
- * created on the first such call on a device and kept; one pipelined call
- * is enqueued at a time per device (a lock). */
+ * joined at its end, and a piece is computed with the same schedule as the
+ * whole call, so the results are the same bits as without pieces.  The
+ * internal streams and events are created on the first such call on a
+ * device and kept; one pipelined call is enqueued at a time per device (a
+ * lock).  A call on a stream that is being captured into a CUDA graph is
+ * not cut (copy, compute, copy on `stream`), so a capture never involves
+ * the shared internal streams. */
 attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
                             float *LSE_host, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                             int window, float sm_scale, attn_dtype_t dtype, void *dev_buf, size_t dev_buf_bytes,

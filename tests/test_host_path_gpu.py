@@ -83,9 +83,10 @@ def test_without_lse_and_on_a_side_stream(attn):
 
 
 def test_graph_capture_replays_with_new_inputs(attn):
-    """The cut call captured in a CUDA graph (the fork to the copy streams
-    and the join are captured too), replayed after the pinned inputs change
-    in place."""
+    """A call large enough to be cut, captured in a CUDA graph (under
+    capture it runs uncut on the stream), replayed after the pinned inputs
+    change in place; meanwhile an eager call on another stream is cut and
+    stays out of the graph."""
     s = CASES[0]
     q, k, v = ai.make_qkv(s, config_id=182)
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -101,6 +102,11 @@ def test_graph_capture_replays_with_new_inputs(attn):
                                 s.Hkv, s.Nq, s.Nk, s.d, s.causal, s.window, s.scale, attn.ATTN_DTYPE_BF16, base, need,
                                 torch.cuda.current_stream().cuda_stream)
         assert st == attn.ATTN_OK
+    # an eager (cut) call while the graph exists: it must not touch the graph's buffers
+    q3, k3, v3 = ai.make_qkv(s, config_id=189)
+    o3, _, _ = host_call(attn, s, q3.pin_memory(), k3.pin_memory(), v3.pin_memory())
+    o3_dev, _ = device_call(attn, s, q3, k3, v3)
+    assert torch.equal(o3, o3_dev.cpu())
     for rep in range(3):
         q2, k2, v2 = ai.make_qkv(s, config_id=183 + rep)
         qh.copy_(q2)

@@ -1378,8 +1378,13 @@ attn_status_t attn_fwd_host(const void *Q_host, const void *K_host, const void *
   attn_status_t st = validate(dQ, dK, dV, dO, dL, s);
   if (st != ATTN_OK) return st;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;
+  // A call captured into a CUDA graph runs unpipelined: the shared copy
+  // streams would otherwise stay in the capture until it ends, and another
+  // thread's call could be captured with it.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return ATTN_ERR_CUDA;
   HostPiece pieces[kHostMaxPieces];
-  const int np = host_pieces(s, pieces);
+  const int np = cap == cudaStreamCaptureStatusNone ? host_pieces(s, pieces) : 0;
   if (np > 0)
     return host_pipelined(static_cast<const uint8_t *>(Q_host), static_cast<const uint8_t *>(K_host),
                           static_cast<const uint8_t *>(V_host), static_cast<uint8_t *>(O_host), LSE_host, s, pieces, np,
