@@ -294,6 +294,11 @@ def workload_calls(name: str):
         # tokens; then the same step with 4 queries per head (speculative decode)
         return [(AttnShape(32, 128, 1, 1, 8192, 512, "bf16", True, 0, 1.0 / math.sqrt(128), mla=True), 11, 0),
                 (AttnShape(8, 128, 1, 4, 8192, 512, "bf16", True, 0, 1.0 / math.sqrt(128), mla=True), 11, 1)]
+    if name == "paged_prefill":
+        # a chunked prefill on a paged cache of 16-token pages: 2048 new query
+        # rows per request against its cache of a drawn length 2048..8192
+        # (the new rows are its last ones), GQA 32/8, d=128, bf16
+        return [(PagedShape(4, 32, 8, 2048, 8192, 128, 16, "bf16", True, 0, None, None, 2048), 12, 0)]
     if name == "paged_decode":
         # one decode step on a paged cache of 16-token pages, bf16, d=128, GQA 32/8:
         # the mqa_decode Hkv=8 call with every request at 8192 tokens (same
@@ -305,4 +310,4 @@ def workload_calls(name: str):
 
 
 WORKLOAD_NAMES = ["mha_n64", "mha_b2h4", "gpt_stack", "gqa_mqa", "long_prefill", "mqa_decode", "mha_n64_bw",
-                  "paged_decode", "mqa_decode_int8", "bwd_gpt_layer", "bwd_gqa", "mla_decode"]
+                  "paged_decode", "mqa_decode_int8", "bwd_gpt_layer", "bwd_gqa", "mla_decode", "paged_prefill"]

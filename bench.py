@@ -52,6 +52,8 @@ WORKLOAD_TEXT = {
     "mqa_decode_int8": "decode B=4, Hq=32, Hkv in {1,8}, Nq=1, Nk=8192, d=128, bf16 Q, int8 K/V (per-tensor scales)",
     "bwd_gpt_layer": "backward of a gpt_stack layer: B=8, H=12, N=2048, d=64, bf16, causal, scale 1/8",
     "bwd_gqa": "backward of B=4, Hq=32, Hkv=8, N=8192, d=128, bf16, causal",
+    "paged_prefill": "chunked prefill on a paged cache (16-token pages, shuffled pool): B=4, Hq=32, Hkv=8, "
+                     "Nq=2048 new rows per request, cache lengths drawn 2048..8192, d=128, bf16, causal",
     "mla_decode": "latent attention with absorbed queries, d_c=512, n_h=128, bf16, causal, scale 1/sqrt(128): "
                   "B=32, Nq=1, Nk=8192; B=8, Nq=4, Nk=8192",
 }
@@ -238,7 +240,7 @@ def prepare_paged(shape, cid, layer, device):
     c["ws"] = torch.empty(wsb, dtype=torch.uint8, device=device)
     path = attn.attn_fwd_paged_path(shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.max_seq_len, shape.d)
     c["path"] = path
-    c["kernel"] = "attn_decode_kernel[paged]"
+    c["kernel"] = "attn_fwd_kernel[paged]" if path == attn.ATTN_PATH_PREFILL else "attn_decode_kernel[paged]"
     c["launches"] = 2 if path == attn.ATTN_PATH_SPLIT_KV else 1
     return c
 

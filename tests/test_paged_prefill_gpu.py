@@ -147,3 +147,23 @@ def test_graph_replay_with_new_lengths(attn, oracle_mod):
         assert attn.device_status() == attn.ATTN_OK
         o_ref, lse_ref = oracle_mod.attention_paged(qn, k, v, table, nl, True)
         pu.compare("bf16", o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref, f"replay {r} {new}")
+
+
+def test_workload_sampled(attn, oracle_mod):
+    """The benchmark's chunked prefill at full size (4 requests, 2048 new rows
+    each, caches of drawn lengths up to 8192): per request, sampled rows
+    against the oracle on the request's cache gathered from its pages."""
+    s, cid, layer = ai.workload_calls("paged_prefill")[0]
+    q, k, v, table, lens = ai.make_paged(s, cid, layer)
+    o, lse = run(attn, s, q, k, v, table, lens)
+    assert attn.device_status() == attn.ATTN_OK
+    ps = s.page_size
+    for b in range(s.B):
+        n = int(lens[b])
+        pages = table[b, :(n + ps - 1) // ps].long()
+        kf = k[pages].permute(1, 0, 2, 3).reshape(s.Hkv, -1, s.d)[:, :n][None].contiguous()
+        vf = v[pages].permute(1, 0, 2, 3).reshape(s.Hkv, -1, s.d)[:, :n][None].contiguous()
+        flat = ai.AttnShape(1, s.Hq, s.Hkv, s.Nq, n, s.d, s.dtype, s.causal, s.window, s.sm_scale)
+        pu.check_sampled(flat, q[b:b + 1], kf, vf, o[b:b + 1], lse[b:b + 1], oracle_mod, count=192, seed=b,
+                         label=f"paged_prefill[{b}]",
+                         config=f"C-paged paged_prefill request {b} of 4 Hq32 Hkv8 Nq2048 L{n} ps16 d128 causal")
