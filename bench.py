@@ -567,10 +567,11 @@ def e2e_timing(calls, steps, warmup, device, stream):
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
-def oracle_sample(workload: str, budget_s: float, seed: int = 0):
+def oracle_sample(workload: str, budget_s: float, seed: int = 0, nthreads: int = 0):
     """Time the fp64 oracle on a bounded, seeded sample of the workload's
-    query rows (every call contributes).  Returns (flops_done, seconds, cores,
-    description)."""
+    query rows (every call contributes).  nthreads = 0: all cores (OpenMP);
+    a positive count is used by the plain forward calls.  Returns
+    (flops_done, seconds, cores, description)."""
     import oracle
 
     oracle.build()
@@ -653,7 +654,7 @@ def oracle_sample(workload: str, budget_s: float, seed: int = 0):
             qr = qf[torch.from_numpy(ids)]
             t0 = time.perf_counter()
             oracle.attention_rows(qr, ids, kf, vf, B=shape.B, Hq=shape.Hq, Nq=shape.Nq, causal=shape.causal,
-                                  window=shape.window, sm_scale=shape.scale)
+                                  window=shape.window, sm_scale=shape.scale, nthreads=nthreads)
             t += time.perf_counter() - t0
         return flops, t
 
@@ -816,6 +817,10 @@ def main():
         f, t, cores, desc = oracle_sample(args.workload, args.cpu_seconds)
         cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
                "seconds": t}
+        if args.workload in ("mha_n64", "mha_b2h4", "mha_n64_bw"):
+            # the small configurations: the same oracle on one core as well
+            f1, t1, _, _ = oracle_sample(args.workload, min(4.0, args.cpu_seconds / 3), seed=1, nthreads=1)
+            cpu["one_core_value"] = f1 / t1 / 1e12
 
     if args.per_call and rank == 0:
         for c, a in zip(calls, avg):
