@@ -238,12 +238,17 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
 
 // Warp-collective wait for a signal that another role of the CTA gives in
 // every case, after an abort too (without work then): it does not poll the
-// abort flag, and its bound is the larger of the wait limit and 1 s.  On
-// that bound it records `code` like any wait and returns false.
+// abort flag.  The signalling role may itself sit in a bounded wait first
+// (3 cycles per nanosecond of the limit, so up to 8x the limit at SM clocks
+// down to 375 MHz), so this bound is the larger of 8x the wait limit and
+// 1 s: running out earlier would let this role run ahead of the other one
+// at their named barriers.  On that bound it records `code` like any wait
+// and returns false.
 __device__ __forceinline__ bool mbar_wait_signal(uint32_t bar, uint32_t parity, const WaitCtl &w, int code) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
-  const uint64_t limit = w.timeout_ns > 1000000000ull ? w.timeout_ns : 1000000000ull;
+  const uint64_t t8 = w.timeout_ns > (1ull << 59) ? ~0ull : 8ull * w.timeout_ns;
+  const uint64_t limit = t8 > 1000000000ull ? t8 : 1000000000ull;
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     if ((it & 31u) == 0 && __any_sync(0xffffffffu, globaltimer_ns() - t0 > limit)) {
