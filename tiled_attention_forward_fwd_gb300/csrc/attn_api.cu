@@ -434,7 +434,7 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   if (launch_pdl(attn_bwd_prep_kernel<D, BF16>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, stream, O,
                  dO, delta, p.dq_acc, rows) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  const dim3 grid(static_cast<unsigned>((s.Nk + 127) / 128), static_cast<unsigned>(zk));
+  const dim3 grid(static_cast<unsigned>(zk), static_cast<unsigned>((s.Nk + 127) / 128));
   if (launch_pdl(attn_bwd_kernel<D, BF16>, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const long long n4 = rows * D / 4;
@@ -1217,7 +1217,7 @@ attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *
   if (st != ATTN_OK) return st;
   if (!dO || !dQ || !dK || !dV || !LSE || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
     return ATTN_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * Hkv > 65535) return ATTN_ERR_INVALID_ARG;  // grid.y
+  if ((static_cast<long long>(Nk) + 127) / 128 > 65535) return ATTN_ERR_INVALID_ARG;  // grid.y: key tiles
   const size_t need = bwd_ws_bytes(static_cast<long long>(B) * Hq * Nq, d);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;

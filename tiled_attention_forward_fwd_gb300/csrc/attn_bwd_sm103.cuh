@@ -14,7 +14,7 @@
 // device memory, as in the forward.
 //
 // GB300 mapping (a synchronous design: each step's MMAs and its elementwise
-// work alternate).  Grid (key tiles of 128 keys, B * Hkv); one thread per
+// work alternate).  Grid (B * Hkv, key tiles of 128 keys); one thread per
 // TMEM lane r (query row, later key row) at d = 128, two at d = 64 (each
 // taking half of the row's columns in the elementwise passes).  A CTA holds K_j and V_j in shared
 // memory and walks every query head of the GQA group and every query tile
@@ -149,8 +149,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_kernel(const 
   const int warp = threadIdx.x >> 5;
   const int row = threadIdx.x & 127;  // TMEM lane: a query row of the tile, later a key row
   const int half = threadIdx.x >> 7;   // which part of the row's columns this thread takes
-  const int kt = blockIdx.x;
-  const int bk = blockIdx.y;  // b * Hkv + kvh
+  // grid (B * Hkv, key tiles): the CTAs start in order of their key tile, so
+  // under a causal mask the longest (first key tiles, every query tile after
+  // them) start first and the shortest end the launch
+  const int kt = blockIdx.y;
+  const int bk = blockIdx.x;  // b * Hkv + kvh
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
   pdl_launch_dependents();
