@@ -280,7 +280,7 @@ size_t attn_fwd_kv_int8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, 
  *   D), not used by an overlapping call; its contents need no
  *   initialisation.  Three kernels are enqueued on `stream` (D and the
  *   accumulator; the gradients; dQ); nothing is allocated; no sync.
- * Errors as attn_fwd_ex; Nk must not exceed 65535 * 128 (key tiles of 128). */
+ * Errors as attn_fwd_ex; B * Hkv * ceil(Nk / 128) must stay below 2^31. */
 attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
                        void *dQ, void *dK, void *dV, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                        int window, float sm_scale, attn_dtype_t dtype, void *workspace, size_t workspace_bytes,

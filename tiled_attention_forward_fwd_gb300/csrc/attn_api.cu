@@ -421,6 +421,10 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.sm_scale = s.sm_scale;
   p.timeout_ns = g_timeout_ns.load();
+  // bands of K/V groups with two waves of CTAs each (at least one group)
+  const long long nkt = (s.Nk + 127) / 128;
+  const long long sms_b = std::max(1, device_sm_count());
+  p.band = static_cast<int>(std::min<long long>(zk, std::max<long long>(1, (2 * sms_b + nkt - 1) / nkt)));
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
   static std::once_flag once[64];
@@ -434,7 +438,7 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   if (launch_pdl(attn_bwd_prep_kernel<D, BF16>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, stream, O,
                  dO, delta, p.dq_acc, rows) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  const dim3 grid(static_cast<unsigned>(zk), static_cast<unsigned>((s.Nk + 127) / 128));
+  const dim3 grid(static_cast<unsigned>(zk * nkt));
   if (launch_pdl(attn_bwd_kernel<D, BF16>, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, p) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const long long n4 = rows * D / 4;
@@ -1217,7 +1221,8 @@ attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *
   if (st != ATTN_OK) return st;
   if (!dO || !dQ || !dK || !dV || !LSE || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
     return ATTN_ERR_INVALID_ARG;
-  if ((static_cast<long long>(Nk) + 127) / 128 > 65535) return ATTN_ERR_INVALID_ARG;  // grid.y: key tiles
+  if (static_cast<long long>(B) * Hkv * ((static_cast<long long>(Nk) + 127) / 128) > 0x7fffffffLL)
+    return ATTN_ERR_INVALID_ARG;  // one CTA per (K/V group, key tile)
   const size_t need = bwd_ws_bytes(static_cast<long long>(B) * Hq * Nq, d);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   if (current_device_sm_major(nullptr) != 10) return ATTN_ERR_UNSUPPORTED;

@@ -14,7 +14,7 @@
 // device memory, as in the forward.
 //
 // GB300 mapping (a synchronous design: each step's MMAs and its elementwise
-// work alternate).  Grid (B * Hkv, key tiles of 128 keys); one thread per
+// work alternate).  One CTA per (K/V group, key tile of 128 keys); one thread per
 // TMEM lane r (query row, later key row) at d = 128, two at d = 64 (each
 // taking half of the row's columns in the elementwise passes).  A CTA holds K_j and V_j in shared
 // memory and walks every query head of the GQA group and every query tile
@@ -61,6 +61,7 @@ struct BwdParams {
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
   unsigned long long timeout_ns;
+  int band;  // K/V groups (b, kvh) per band of the CTA order
 };
 
 template <int D>
@@ -149,11 +150,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_kernel(const 
   const int warp = threadIdx.x >> 5;
   const int row = threadIdx.x & 127;  // TMEM lane: a query row of the tile, later a key row
   const int half = threadIdx.x >> 7;   // which part of the row's columns this thread takes
-  // grid (B * Hkv, key tiles): the CTAs start in order of their key tile, so
-  // under a causal mask the longest (first key tiles, every query tile after
-  // them) start first and the shortest end the launch
-  const int kt = blockIdx.y;
-  const int bk = blockIdx.x;  // b * Hkv + kvh
+  // A 1-D grid over (K/V group, key tile) in bands of p.band groups: a band's
+  // CTAs start in order of their key tile, so that under a causal mask the
+  // longest (first key tiles, which every later query tile reaches) start
+  // first and the band ends with its shortest, and the CTAs in flight read
+  // the Q and dO of one band's groups (a few in L2) rather than of all.
+  const int nkt = (p.Nk + 127) / 128;
+  const int zk = p.B * p.Hkv;
+  const int per_band = p.band * nkt;
+  const int band = static_cast<int>(blockIdx.x) / per_band;
+  const int r = static_cast<int>(blockIdx.x) - band * per_band;
+  const int gb = min(p.band, zk - band * p.band);  // groups in this band (the last may hold fewer)
+  const int kt = r / gb;
+  const int bk = band * p.band + (r - kt * gb);  // b * Hkv + kvh
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
   pdl_launch_dependents();
