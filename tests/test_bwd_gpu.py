@@ -115,6 +115,9 @@ CASES = [
     ai.AttnShape(1, 2, 2, 700, 700, 128, "bf16", True, 300),
     ai.AttnShape(1, 8, 1, 384, 384, 128, "bf16", False),     # MQA
     ai.AttnShape(2, 2, 2, 129, 129, 128, "fp16", True),      # one key past a tile
+    # 23 K/V groups x 16 key tiles: on a 152-SM part the CTAs form bands of
+    # ceil(304 / 16) = 19 groups, the last band holding 4
+    ai.AttnShape(23, 1, 1, 2048, 2048, 64, "bf16", True),
 ]
 
 
