@@ -287,6 +287,15 @@ attn_status_t attn_bwd(const void *Q, const void *K, const void *V, const void *
                        cudaStream_t stream);
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq, int d);
 
+/* The backward kernel's CTA order for these sizes on a device of `sms` SMs,
+ * without device work: one CTA per (K/V group bk = b * Hkv + kvh, key tile
+ * kt of 128 keys), in bands of ceil(2 * sms / key tiles) groups (two waves),
+ * within a band in key-tile order (under a causal mask the longest first;
+ * lab 02, "La estructura del kernel": one program per head and tile).
+ * tiles (HOST, 2 ints per CTA, written up to max_ctas CTAs): {bk, kt} in
+ * launch order.  Returns the CTA count, or -1 for bad sizes. */
+int attn_bwd_cta_order(int B, int Hkv, int Nk, int sms, int *tiles, int max_ctas);
+
 /* Attention over a latent K/V cache with absorbed queries (Multi-Head
  * Latent Attention; cruxr.ai "Optimizaciones de Atencion", section
  * "Multi-Head Latent Attention (MLA)").  Each token caches one latent vector

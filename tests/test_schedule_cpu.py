@@ -195,3 +195,35 @@ def test_truncated_buffer(attn):
     n = L.attn_fwd_prefill_visits(1, 4, 4, 700, 700, 64, 1, 0, 0, 152, info, buf, 3)
     assert n > 3
     assert all(buf[x] != -7 for x in range(18)) and all(buf[x] == -7 for x in range(18, 24))
+
+
+@pytest.mark.parametrize("B,Hkv,Nk,sms", [(4, 8, 8192, 152), (8, 12, 2048, 152), (23, 1, 2048, 152), (1, 1, 100, 152),
+                                          (3, 5, 1000, 7), (2, 3, 130, 1)])
+def test_bwd_cta_order(attn, B, Hkv, Nk, sms):
+    """The backward's CTAs: every (K/V group, key tile) once; groups in bands
+    of ceil(2 * sms / key tiles) (two waves of CTAs, the last band the rest);
+    within a band the key tiles in order, so under a causal mask a CTA never
+    starts before one with more query tiles to walk (lab 02, "La estructura
+    del kernel": one program per head and tile)."""
+    order = attn.attn_bwd_cta_order(B, Hkv, Nk, sms)
+    zk, nkt = B * Hkv, -(-Nk // BN)
+    assert order.shape == (zk * nkt, 2)
+    assert len({(g, t) for g, t in order.tolist()}) == zk * nkt
+    assert order[:, 0].min() == 0 and order[:, 0].max() == zk - 1 and order[:, 1].max() == nkt - 1
+    band = min(zk, max(1, -(-2 * sms // nkt)))
+    c = 0
+    for first in range(0, zk, band):
+        groups = list(range(first, min(zk, first + band)))
+        part = order[c:c + len(groups) * nkt]
+        c += len(groups) * nkt
+        assert sorted(set(part[:, 0].tolist())) == groups
+        assert (np.diff(part[:, 1]) >= 0).all()
+        for t in range(nkt):
+            assert sorted(part[part[:, 1] == t, 0].tolist()) == groups
+    assert c == zk * nkt
+
+
+def test_bwd_cta_order_bad_sizes(attn):
+    assert attn.attn_bwd_cta_order(0, 1, 128, 152) is None
+    assert attn.attn_bwd_cta_order(1, 1, 128, 0) is None
+    assert attn.attn_bwd_cta_order(65536, 256, 1 << 20, 152) is None  # more than 2^31 CTAs

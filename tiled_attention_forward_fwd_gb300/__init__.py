@@ -37,7 +37,8 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_workspace_bytes", "attn_fwd_hos
             "attn_fwd_decode_noalloc", "attn_fwd_path", "attn_fwd_prefill_visits", "attn_fwd_paged",
             "attn_fwd_paged_workspace_bytes", "attn_fwd_paged_path",
             "attn_fwd_decode_plan", "attn_set_test_stall", "attn_fwd_kv_int8", "attn_bwd", "attn_bwd_workspace_bytes",
-            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes", "attn_empty_launch", "attn_fwd_kv_int8_workspace_bytes"]
+            "attn_fwd_mla", "attn_fwd_mla_workspace_bytes", "attn_empty_launch", "attn_fwd_kv_int8_workspace_bytes",
+            "attn_bwd_cta_order"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.restype = ci
         L.attn_bwd_workspace_bytes.argtypes = [ci] * 4
         L.attn_bwd_workspace_bytes.restype = sz
+        L.attn_bwd_cta_order.argtypes = [ci, ci, ci, ci, ctypes.POINTER(ci), ci]
+        L.attn_bwd_cta_order.restype = ci
         L.attn_fwd_mla.argtypes = [vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp, sz, vp]
         L.attn_fwd_mla.restype = ci
         L.attn_fwd_mla_workspace_bytes.argtypes = [ci] * 5
@@ -189,6 +192,20 @@ def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Nq, Nk, d, causal, win
 
 def attn_bwd_workspace_bytes(B, Hq, Nq, d) -> int:
     return int(lib().attn_bwd_workspace_bytes(B, Hq, Nq, d))
+
+
+def attn_bwd_cta_order(B, Hkv, Nk, sms):
+    """The backward kernel's CTA order: an int array (CTAs, 2) of (K/V group,
+    key tile) in launch order, or None for bad sizes."""
+    import numpy as np
+
+    n = int(lib().attn_bwd_cta_order(B, Hkv, Nk, sms, None, 0))
+    if n < 0:
+        return None
+    out = np.zeros((n, 2), dtype=np.int32)
+    got = int(lib().attn_bwd_cta_order(B, Hkv, Nk, sms, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n))
+    assert got == n
+    return out
 
 
 def attn_fwd_mla(Q_lat, C_lat, O_lat, LSE, B, n_h, Nq, Nk, d_c, causal, window, sm_scale, dtype, workspace,

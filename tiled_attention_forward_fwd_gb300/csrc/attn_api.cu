@@ -421,10 +421,8 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   p.scale_log2 = static_cast<float>(static_cast<double>(s.sm_scale) * 1.4426950408889634074);
   p.sm_scale = s.sm_scale;
   p.timeout_ns = g_timeout_ns.load();
-  // bands of K/V groups with two waves of CTAs each (at least one group)
   const long long nkt = (s.Nk + 127) / 128;
-  const long long sms_b = std::max(1, device_sm_count());
-  p.band = static_cast<int>(std::min<long long>(zk, std::max<long long>(1, (2 * sms_b + nkt - 1) / nkt)));
+  p.band = bwd_band(zk, nkt, std::max(1, device_sm_count()));
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
   static std::once_flag once[64];
@@ -1438,6 +1436,21 @@ const char *attn_status_string(attn_status_t status) {
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+int attn_bwd_cta_order(int B, int Hkv, int Nk, int sms, int *tiles, int max_ctas) {
+  if (B <= 0 || Hkv <= 0 || Nk <= 0 || sms <= 0 || (max_ctas > 0 && tiles == nullptr)) return -1;
+  const long long zk = static_cast<long long>(B) * Hkv, nkt = (static_cast<long long>(Nk) + 127) / 128;
+  if (zk * nkt > 0x7fffffffLL) return -1;
+  const int band = bwd_band(zk, nkt, sms);
+  const int n = static_cast<int>(zk * nkt);
+  for (int c = 0; c < n && c < max_ctas; ++c) {
+    int bk = 0, kt = 0;
+    bwd_cta_tile(c, band, static_cast<int>(zk), static_cast<int>(nkt), bk, kt);
+    tiles[2 * c] = bk;
+    tiles[2 * c + 1] = kt;
+  }
+  return n;
+}
 
 attn_status_t attn_empty_launch(int grid, int threads, size_t smem_bytes, cudaStream_t stream) {
   if (grid <= 0 || threads <= 0 || threads > 1024 || smem_bytes > 232448) return ATTN_ERR_INVALID_ARG;

@@ -38,6 +38,7 @@
 // pre-pass computes D and zeroes the dQ accumulator; a post-pass writes dQ.
 #pragma once
 
+#include "fastdiv.h"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -63,6 +64,26 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int band;  // K/V groups (b, kvh) per band of the CTA order
 };
+
+// The CTA order: one CTA per (K/V group bk = b * Hkv + kvh, key tile kt), in
+// bands of `band` groups; within a band the CTAs go in order of their key
+// tile, so under a causal mask the longest (first key tiles, which every
+// later query tile reaches) start first and the band ends with its
+// shortest, while the CTAs in flight read the Q and dO of one band's groups
+// (a few in L2) rather than of all.  Two waves of CTAs per band.
+ATTN_HD int bwd_band(long long zk, long long nkt, long long sms) {
+  const long long w = (2 * (sms > 0 ? sms : 1) + nkt - 1) / nkt;
+  return static_cast<int>(w < 1 ? 1 : (w < zk ? w : zk));
+}
+// CTA `cta` (launch order) of zk groups x nkt key tiles in bands of `band`.
+ATTN_HD void bwd_cta_tile(int cta, int band, int zk, int nkt, int &bk, int &kt) {
+  const int per_band = band * nkt;
+  const int bd = cta / per_band;
+  const int r = cta - bd * per_band;
+  const int gb = band < zk - bd * band ? band : zk - bd * band;  // groups in this band (the last may hold fewer)
+  kt = r / gb;
+  bk = bd * band + (r - kt * gb);
+}
 
 template <int D>
 struct BwdCfg {
@@ -150,19 +171,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_kernel(const 
   const int warp = threadIdx.x >> 5;
   const int row = threadIdx.x & 127;  // TMEM lane: a query row of the tile, later a key row
   const int half = threadIdx.x >> 7;   // which part of the row's columns this thread takes
-  // A 1-D grid over (K/V group, key tile) in bands of p.band groups: a band's
-  // CTAs start in order of their key tile, so that under a causal mask the
-  // longest (first key tiles, which every later query tile reaches) start
-  // first and the band ends with its shortest, and the CTAs in flight read
-  // the Q and dO of one band's groups (a few in L2) rather than of all.
-  const int nkt = (p.Nk + 127) / 128;
-  const int zk = p.B * p.Hkv;
-  const int per_band = p.band * nkt;
-  const int band = static_cast<int>(blockIdx.x) / per_band;
-  const int r = static_cast<int>(blockIdx.x) - band * per_band;
-  const int gb = min(p.band, zk - band * p.band);  // groups in this band (the last may hold fewer)
-  const int kt = r / gb;
-  const int bk = band * p.band + (r - kt * gb);  // b * Hkv + kvh
+  // a 1-D grid in the order of bwd_cta_tile
+  int kt, bk;  // key tile; K/V group b * Hkv + kvh
+  bwd_cta_tile(static_cast<int>(blockIdx.x), p.band, p.B * p.Hkv, (p.Nk + 127) / 128, bk, kt);
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
   WaitCtl wc{abort_flag, p.status, p.timeout_ns};
   pdl_launch_dependents();
