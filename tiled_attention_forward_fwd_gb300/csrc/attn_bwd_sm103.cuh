@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_kernel(const 
       // columns in the 128-byte swizzle (16-byte chunk q of row r at q ^ (r
       // % 8): no bank conflicts), then one TMA reduce-add per box.  Rows past
       // Nq are clipped by the tensor map.
-#pragma unroll
+#pragma unroll 1  // rolled: 7.92 -> 7.83 ms on bwd_gqa (d = 64 takes one box a thread)
       for (int c2 = 0; c2 < D / 32 / C::kPerLane; ++c2) {
         const int cc = half * (D / 32 / C::kPerLane) + c2;  // this thread's 32-column boxes
         uint32_t r[32];
