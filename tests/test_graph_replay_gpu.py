@@ -125,3 +125,39 @@ def test_paged_replays_with_new_lengths(attn, oracle_mod, Hq, Hkv, d, kind):
         assert attn.device_status() == attn.ATTN_OK
         o_ref, lse_ref = oracle_mod.attention_paged(qn, k, v, table, nl, True)
         pu.compare("bf16", o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref, f"paged replay {r} {new_lens}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_replays(attn, d):
+    """The backward (a pre-pass that zeroes the dQ accumulator, the kernel that
+    reduce-adds every key tile's dQ part into it, then the dQ pass) captured
+    once and replayed with a new dO written in place each time: every replay
+    equals an eager call on the same inputs (the accumulator starts from
+    zero in every replay), up to the order in which the CTAs' fp32
+    reduce-adds land."""
+    s = ai.AttnShape(2, 4, 2, 600, 600, d, "bf16", True)
+    q, k, v = (t.cuda() for t in ai.make_qkv(s, config_id=195))
+    o, lse = attn.flash_attn_forward(q, k, v, causal=True)
+    do = torch.empty_like(q)
+    ws = torch.empty(attn.attn_bwd_workspace_bytes(s.B, s.Hq, s.Nq, s.d), dtype=torch.uint8, device="cuda")
+    out = {}
+
+    def call():
+        out["g"] = attn.flash_attn_backward(q, k, v, o, lse, do, True, workspace=ws)
+
+    do.copy_(ai.normal_tensor(ai.seed_for(195, 0, "G"), tuple(q.shape), s.dtype).cuda())
+    g = capture(call)
+    for r in range(REPLAYS):
+        do.copy_(ai.normal_tensor(ai.seed_for(195, r + 1, "G"), tuple(q.shape), s.dtype).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert attn.device_status() == attn.ATTN_OK
+        got = [t.clone() for t in out["g"]]
+        want = attn.flash_attn_backward(q, k, v, o, lse, do, True)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("dQ", "dK", "dV"), got, want):
+            assert torch.isfinite(a.float()).all(), (r, name)
+            # the reduce-adds of different CTAs may land in another order
+            # in the two launches (fp32 sums): compare within the rounding
+            # of a few fp32 additions on top of the 16-bit output
+            torch.testing.assert_close(a.float(), b.float(), rtol=2e-2, atol=2e-3, msg=f"replay {r} {name}")
