@@ -217,6 +217,7 @@ static bool prefill_kernel_ready(int dev, int sched, bool paged = false) {
     ok[k][dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       FwdCfg<D>::kSmemBytes) == cudaSuccess &&
                  cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs == kLaunchRegs;
+    if (!ok[k][dev]) (void)cudaGetLastError();  // not reported by a later launch check
   });
   return ok[k][dev];
 }
@@ -430,6 +431,7 @@ static attn_status_t launch_bwd(const void *Q, const void *K, const void *V, con
   std::call_once(once[dev], [&] {
     ready[dev] = cudaFuncSetAttribute(attn_bwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg::kSmemBytes) == cudaSuccess;
+    if (!ready[dev]) (void)cudaGetLastError();
   });
   if (!ready[dev]) return ATTN_ERR_UNSUPPORTED;
   float *delta = reinterpret_cast<float *>(base + round_up256(static_cast<size_t>(rows) * D * 4));
@@ -517,6 +519,7 @@ static attn_status_t launch_mla(const void *Q, const void *Cl, void *O, float *L
                                       MlaCfg::kSmemBytes) == cudaSuccess &&
                  cudaFuncSetAttribute(attn_mla_kernel<!BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       MlaCfg::kSmemBytes) == cudaSuccess;
+    if (!ready[dev]) (void)cudaGetLastError();
   });
   if (!ready[dev]) return ATTN_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(pl.nchunks), static_cast<unsigned>(static_cast<long long>(s.B) * pl.row_blocks));
@@ -602,6 +605,7 @@ static attn_status_t launch_mla_tc(const void *Q, const void *Cl, void *O, float
                                       MlaTcCfg::kSmemBytes) == cudaSuccess &&
                  cudaFuncSetAttribute(attn_mla_tc_kernel<!BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       MlaTcCfg::kSmemBytes) == cudaSuccess;
+    if (!ready[dev]) (void)cudaGetLastError();
   });
   if (!ready[dev]) return ATTN_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(2 * pl.nchunks),
@@ -639,18 +643,23 @@ static int decode_ctas_per_sm_t() {
   static int cache[64];
   static std::once_flag once[64];
   std::call_once(once[dev], [&] {
+    bool bad = false;
     for (auto k : {attn_decode_kernel<D, true, RB, false>, attn_decode_kernel<D, false, RB, false>,
                    attn_decode_kernel<D, true, RB, true>, attn_decode_kernel<D, false, RB, true>})
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+      bad |= cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess;
     for (auto k : {attn_decode_kernel<D, true, RB, false, true>, attn_decode_kernel<D, false, RB, false, true>})
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D, RB, true>::kSmemBytes);
+      bad |= cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D, RB, true>::kSmemBytes) !=
+             cudaSuccess;
     // flat and paged kernels: the smaller residency (the plan sizes one wave)
     int n = 0, n_paged = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<D, true, RB, false>, kDecThreads,
                                                       Cfg::kSmemBytes) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n_paged, attn_decode_kernel<D, true, RB, true>, kDecThreads,
-                                                      Cfg::kSmemBytes) != cudaSuccess)
+                                                      Cfg::kSmemBytes) != cudaSuccess) {
       n = 0;
+      bad = true;
+    }
+    if (bad) (void)cudaGetLastError();  // not reported by a later launch check
     n = std::min(n, n_paged);
     cache[dev] = n;
   });
@@ -865,12 +874,15 @@ static int short_ctas_per_sm() {
   static int cache[64];
   static std::once_flag once[64];
   std::call_once(once[dev], [&] {
-    cudaFuncSetAttribute(attn_short_kernel<D, BF16, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Cfg::kSmemBytes);
+    bool bad = cudaFuncSetAttribute(attn_short_kernel<D, BF16, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::kSmemBytes) != cudaSuccess;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_short_kernel<D, BF16, NK>, kShortThreads,
-                                                      Cfg::kSmemBytes) != cudaSuccess)
+                                                      Cfg::kSmemBytes) != cudaSuccess) {
       n = 0;
+      bad = true;
+    }
+    if (bad) (void)cudaGetLastError();  // not reported by a later launch check
     cache[dev] = n;
   });
   return cache[dev];
@@ -1461,6 +1473,7 @@ attn_status_t attn_empty_launch(int grid, int threads, size_t smem_bytes, cudaSt
   std::call_once(once[dev], [&] {
     ready[dev] = cudaFuncSetAttribute(attn::attn_empty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       232448) == cudaSuccess;
+    if (!ready[dev]) (void)cudaGetLastError();
   });
   if (!ready[dev]) return ATTN_ERR_CUDA;
   if (attn::launch_pdl(attn::attn_empty_kernel, dim3(static_cast<unsigned>(grid)), dim3(static_cast<unsigned>(threads)),
