@@ -980,10 +980,12 @@ static attn_status_t run(const void *Q, const void *K, const void *V, void *O, f
 // A large call on host buffers is cut into pieces: contiguous ranges of
 // (request, K/V head) slabs, each a contiguous byte range of Q, K, V, O and
 // LSE and a call of its own.  A piece's inputs are copied in on one internal
-// stream, its kernel runs on the caller's stream once they have arrived, and
-// its outputs are copied out on a second internal stream: the copies of one
-// piece overlap the compute of its neighbours (copy-in, compute and copy-out
-// each go in piece order).  Pieces are used only when each is computed with
+// stream, its kernel runs once they have arrived (even pieces on the
+// caller's stream, odd ones on an internal compute stream, so that a piece's
+// CTAs can start on the SMs the previous piece's last CTAs leave idle), and
+// its outputs are copied out on another internal stream: the copies of one
+// piece overlap the compute of its neighbours (copy-in and copy-out each go
+// in piece order).  Pieces are used only when each is computed with
 // the schedule and item shape of the whole call (the plain prefill, the same
 // pairing of query tiles), so the results are the same bits.
 constexpr int kHostMaxPieces = 16;
@@ -995,12 +997,13 @@ struct HostPiece {
   int h0, nh;  // K/V heads [h0, h0 + nh) of each (all of them when nb > 1)
 };
 
-// Per device: two copy streams and the events that chain the pieces.
+// Per device: two copy streams, a second compute stream and the events that
+// chain the pieces.
 struct HostPipe {
   std::mutex mu;  // one pipelined enqueue at a time per device (the events are shared)
   bool ready = false;
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_comp = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_comp_end = nullptr;
   cudaEvent_t ev_in[kHostMaxPieces] = {}, ev_comp[kHostMaxPieces] = {};
 };
 
@@ -1016,8 +1019,10 @@ static bool host_pipe_init(HostPipe &hp) {
   if (hp.ready) return true;
   bool ok = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.s_comp, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&hp.ev_end, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&hp.ev_end, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.ev_comp_end, cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < kHostMaxPieces; ++i)
     ok = cudaEventCreateWithFlags(&hp.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&hp.ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
@@ -1032,10 +1037,12 @@ static bool host_pipe_init(HostPipe &hp) {
   }
   if (hp.ev_start) cudaEventDestroy(hp.ev_start);
   if (hp.ev_end) cudaEventDestroy(hp.ev_end);
+  if (hp.ev_comp_end) cudaEventDestroy(hp.ev_comp_end);
   if (hp.s_in) cudaStreamDestroy(hp.s_in);
   if (hp.s_out) cudaStreamDestroy(hp.s_out);
-  hp.ev_start = hp.ev_end = nullptr;
-  hp.s_in = hp.s_out = nullptr;
+  if (hp.s_comp) cudaStreamDestroy(hp.s_comp);
+  hp.ev_start = hp.ev_end = hp.ev_comp_end = nullptr;
+  hp.s_in = hp.s_out = hp.s_comp = nullptr;
   cudaGetLastError();
   return false;
 }
@@ -1081,9 +1088,9 @@ static int host_pieces(const Shape &s, HostPiece *out) {
 
 // Enqueues the pieces of a host-buffer call (device buffers dQ..dL hold the
 // whole call; host pointers are its host arrays).  `stream` is forked to the
-// two copy streams at the start and joined at the end, so the call as a
-// whole still follows and precedes the work around it on `stream` (also
-// under CUDA-graph capture).  On a CUDA error the streams are still joined.
+// two copy streams and the second compute stream at the start and joined at
+// the end, so the call as a whole still follows and precedes the work around
+// it on `stream`.  On a CUDA error the streams are still joined.
 static attn_status_t host_pipelined(const uint8_t *Qh, const uint8_t *Kh, const uint8_t *Vh, uint8_t *Oh,
                                     float *Lh, const Shape &s, const HostPiece *pc, int np, uint8_t *dQ,
                                     uint8_t *dK, uint8_t *dV, uint8_t *dO, float *dL, cudaStream_t stream) {
@@ -1097,7 +1104,8 @@ static attn_status_t host_pipelined(const uint8_t *Qh, const uint8_t *Kh, const 
   const size_t kvh_bytes = static_cast<size_t>(s.Nk) * s.d * 2;  // one K/V head
   bool ok = cudaEventRecord(hp.ev_start, stream) == cudaSuccess &&
             cudaStreamWaitEvent(hp.s_in, hp.ev_start, 0) == cudaSuccess &&
-            cudaStreamWaitEvent(hp.s_out, hp.ev_start, 0) == cudaSuccess;
+            cudaStreamWaitEvent(hp.s_out, hp.ev_start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.s_comp, hp.ev_start, 0) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;
@@ -1105,6 +1113,9 @@ static attn_status_t host_pipelined(const uint8_t *Qh, const uint8_t *Kh, const 
   attn_status_t st = ATTN_OK;
   for (int i = 0; i < np && ok && st == ATTN_OK; ++i) {
     const HostPiece &p = pc[i];
+    // odd pieces compute on the second stream: a piece's kernel can take
+    // the SMs that the previous piece's last CTAs leave idle
+    cudaStream_t cs = (i & 1) ? hp.s_comp : stream;
     const size_t q0 = static_cast<size_t>(p.b0) * s.Hq + static_cast<size_t>(p.h0) * g;  // first query head
     const size_t nq = static_cast<size_t>(p.nb) * p.nh * g;                                // query heads
     const size_t k0 = static_cast<size_t>(p.b0) * s.Hkv + p.h0;                          // first K/V head
@@ -1116,23 +1127,26 @@ static attn_status_t host_pipelined(const uint8_t *Qh, const uint8_t *Kh, const 
          cudaMemcpyAsync(dV + k0 * kvh_bytes, Vh + k0 * kvh_bytes, nkv * kvh_bytes, cudaMemcpyHostToDevice,
                          hp.s_in) == cudaSuccess &&
          cudaEventRecord(hp.ev_in[i], hp.s_in) == cudaSuccess &&
-         cudaStreamWaitEvent(stream, hp.ev_in[i], 0) == cudaSuccess;
+         cudaStreamWaitEvent(cs, hp.ev_in[i], 0) == cudaSuccess;
     if (!ok) break;
     const Shape ps{p.nb, p.nh * g, p.nh, s.Nq, s.Nk, s.d, s.causal, s.window, s.sm_scale, s.dtype};
     float *dLp = dL ? dL + q0 * s.Nq : nullptr;
     st = run(dQ + q0 * qh_bytes, dK + k0 * kvh_bytes, dV + k0 * kvh_bytes, dO + q0 * qh_bytes, dLp, ps, nullptr, 0,
-             stream);
+             cs);
     if (st != ATTN_OK) break;
-    ok = cudaEventRecord(hp.ev_comp[i], stream) == cudaSuccess &&
+    ok = cudaEventRecord(hp.ev_comp[i], cs) == cudaSuccess &&
          cudaStreamWaitEvent(hp.s_out, hp.ev_comp[i], 0) == cudaSuccess &&
          cudaMemcpyAsync(Oh + q0 * qh_bytes, dO + q0 * qh_bytes, nq * qh_bytes, cudaMemcpyDeviceToHost,
                          hp.s_out) == cudaSuccess &&
          (Lh == nullptr || cudaMemcpyAsync(Lh + q0 * s.Nq, dLp, nq * s.Nq * sizeof(float), cudaMemcpyDeviceToHost,
                                            hp.s_out) == cudaSuccess);
   }
-  // join both copy streams back into `stream`, also after an error
+  // join the copy streams and the second compute stream back into
+  // `stream`, also after an error
   const bool joined = cudaEventRecord(hp.ev_end, hp.s_out) == cudaSuccess &&
                       cudaStreamWaitEvent(stream, hp.ev_end, 0) == cudaSuccess &&
+                      cudaEventRecord(hp.ev_comp_end, hp.s_comp) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, hp.ev_comp_end, 0) == cudaSuccess &&
                       cudaEventRecord(hp.ev_start, hp.s_in) == cudaSuccess &&
                       cudaStreamWaitEvent(stream, hp.ev_start, 0) == cudaSuccess;
   if (st != ATTN_OK) return st;
